@@ -1,0 +1,433 @@
+"""Bench: layout -> dispatch -> combine of one EP layer on GB300.
+
+One step = one pass of the whole hot path (ep_layout, ep_dispatch with its
+TransferCmd rings, ep_combine) over the workload's synthetic batch, with all
+inputs resident in HBM.  The L2 is flushed between steps (a write of twice its
+size, outside the timed events); per-step time is the sum of CUDA-event
+intervals on the launching stream.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload ht]
+  python bench.py --impl reference ...   # the CPU oracle on the host, same metric
+
+Multi-GPU: the path does not shard across GPUs here (each simulated EP group
+lives in one GPU's memory), so N GPUs run N independent replicas; `value` is
+the bytes all replicas moved divided by the slowest replica's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "dispatch+combine µs per EP layer and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+WORKLOAD_TEXT = {
+    "ht": "high-throughput DeepSeek-V3 shape: 32 ranks x 4096 tokens, hidden 7168 bf16, 256 experts, "
+          "top-8 uniform, 8 channels, batches of 8 TransferCmds",
+    "ll": "low-latency DeepSeek-V3 shape: 32 ranks x 128 tokens, hidden 7168 bf16, 256 experts, top-8 uniform",
+    "skew": "skewed routing: 16 ranks x 8192 tokens, hidden 2048 bf16, 64 experts, top-6 Zipf(1.2)",
+    "small": "small-message packing: 32 ranks x 2048 tokens, hidden 1024 bf16, 128 experts, top-4, 8 rows/msg",
+    "tiny": "tiny: 4 ranks x 16 tokens, hidden 256, 16 experts, top-2",
+}
+
+
+# --------------------------------------------------------------------- bytes
+def algorithmic_bytes(R, T, H, E, K, n_recv, n_msgs, n_sent):
+    """Bytes each op must move (reads + writes), excluding re-reads."""
+    B = 2 * H
+    small = R * E * 4 + 5 * R * R * 4 + 2 * R * 4 + E * 4
+    layout = T * K * 4 + T * R * (1 + 4) + small
+    dispatch = n_sent * B + n_recv * B + T * R * 4 + n_msgs * 32
+    combine = n_recv * B + T * B + T * K * 8 + T * R * 4
+    return {"layout": layout, "dispatch": dispatch, "combine": combine}
+
+
+def read_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def read_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
+    was taken on the current source of that kernel (else None)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    src = os.path.join(ROOT, "combine_ep_layout_04_gb300", "csrc", f"ep_{kernel}.cu")
+    if not os.path.exists(path) or not os.path.exists(src):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for line in open(path):
+        if line.startswith("#") or "=" not in line:
+            continue
+        kv = dict(tok.split("=", 1) for tok in line.split())
+        if kv.get("kernel") == kernel and kv.get("workload") == workload and kv.get("src_sha") == sha:
+            return int(float(kv["dram_bytes_per_launch"]))
+    return None
+
+
+# -------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) tagged with host time; summarised over the
+    timed window only."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [v.strip() for v in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        rows = [r for (t, r) in self.rows if t0 <= t <= t1 + 0.25]
+        if not rows:
+            rows = [r for (_, r) in self.rows[-3:]]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        try:
+            sm = [float(r[2]) for r in rows]
+            smax = max(float(r[3]) for r in rows)
+        except ValueError:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unparsed"], "samples": len(rows)}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": smax, "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[4]) for r in rows if r[4] not in ("", "[N/A]"))}
+
+
+# ---------------------------------------------------------------- CPU oracle
+def cpu_oracle_rates(w, idx, wt, x_dev, eo_dev, budget_s: float = 12.0):
+    """Time the oracle (single thread) on a bounded sample of the workload:
+    the full layout, the dispatch of one source rank's tokens, and the combine
+    of a token sample.  Returns per-op GB/s of algorithmic bytes and a note."""
+    import torch
+
+    import oracle
+    R, Tpr, H, E, K = w.num_ranks, w.tokens_per_rank, w.hidden, w.num_experts, w.topk
+    T, B = w.num_tokens, 2 * w.hidden
+    G = oracle.default_rows_per_msg(H)
+    t0 = time.perf_counter()
+    lay = oracle.layout(R, Tpr, E, idx, G)
+    t_layout = time.perf_counter() - t0
+    N = lay["n_recv"]
+    n_msgs = int(lay["msg_count"].sum())
+    full = algorithmic_bytes(R, T, H, E, K, N, n_msgs, T)
+    rates = {"layout": full["layout"] / t_layout / 1e9}
+    # dispatch: source ranks' tokens until about a third of the budget
+    recv = np.empty((N, H), np.uint16)
+    done_tok, t_disp, bytes_disp = 0, 0.0, 0
+    while done_tok < T and t_disp < budget_s / 3:
+        t1 = min(T, done_tok + Tpr)
+        xs = x_dev[done_tok:t1].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        c0 = time.perf_counter()
+        oracle.dispatch(lay, xs, done_tok, t1, recv=recv, x_first_token=done_tok)
+        t_disp += time.perf_counter() - c0
+        rows = int((lay["token_slot"][done_tok:t1] >= 0).sum())
+        bytes_disp += (t1 - done_tok) * B + rows * B + (t1 - done_tok) * R * 4 + rows // G * 32
+        done_tok = t1
+    rates["dispatch"] = bytes_disp / t_disp / 1e9
+    # combine: a token sample, reading only the rows it needs
+    ntok = 256
+    rng = np.random.default_rng(0)
+    toks = np.sort(rng.choice(T, min(T, ntok), replace=False))
+    need = sorted({int(lay["recv_base"][d]) + int(lay["token_slot"][t, d])
+                   for t in toks for d in range(R) if lay["token_slot"][t, d] >= 0})
+    eo = eo_dev.index_select(0, torch.tensor(need, device=eo_dev.device)).view(torch.int16).cpu().numpy().view(np.uint16)
+    pos = {r: i for i, r in enumerate(need)}
+    sub = np.full((len(toks), R), -1, np.int32)
+    for i, t in enumerate(toks):
+        for d in range(R):
+            if lay["token_slot"][t, d] >= 0:
+                sub[i, d] = pos[int(lay["recv_base"][d]) + int(lay["token_slot"][t, d])]
+    c0 = time.perf_counter()
+    oracle.combine({"token_slot": sub, "recv_base": np.zeros(R, np.int32)}, idx[toks], wt[toks], E // R, eo)
+    t_comb = time.perf_counter() - c0
+    bytes_comb = len(need) * B + len(toks) * B + len(toks) * K * 8 + len(toks) * R * 4
+    rates["combine"] = bytes_comb / t_comb / 1e9
+    note = (f"oracle, 1 thread: full layout; dispatch of {done_tok} tokens ({done_tok // Tpr} source ranks); "
+            f"combine of {len(toks)} tokens; GB/s per op scaled to the full step")
+    return rates, full, note
+
+
+def step_rate(full: dict, rates: dict) -> tuple[float, float]:
+    """(GB/s over the whole step, seconds per step) at the given per-op rates."""
+    secs = sum(full[k] / (rates[k] * 1e9) for k in full)
+    return sum(full.values()) / secs / 1e9, secs
+
+
+# ---------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="ht", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3 or os.environ.get("EP_BENCH_ALLOW_SHORT_WARMUP"), "warm-up must be >= 3 steps"
+
+    import torch
+
+    import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = W.get(args.workload)
+
+    if args.impl == "reference":
+        return run_reference(args, w, world, rank)
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl", device_id=dev)
+
+    from combine_ep_layout_04_gb300 import EpLayer
+
+    R, Tpr, H, E, K = w.num_ranks, w.tokens_per_rank, w.hidden, w.num_experts, w.topk
+    T = w.num_tokens
+    idx, wt = W.make_routing(w)
+    x = W.make_x_torch(w, dev)
+    topk = torch.from_numpy(idx).to(dev)
+    wts = torch.from_numpy(wt).to(dev)
+    layer = EpLayer(R, Tpr, H, E, K, channels=w.channels, ring_depth=w.ring_depth, max_inflight=w.max_inflight,
+                    rows_per_msg=w.rows_per_msg, device=dev)
+    lay = layer.layout(topk)            # sizes recv once; every step recomputes the layout
+    N = lay.n_recv
+    recv = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+    eo = W.make_expert_out_torch(N, H, dev, w.seed)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    n_msgs = int(lay.msg_count.sum())
+    n_sent = int((lay.is_token_in_rank.sum(dim=1) > 0).sum())
+    ab = algorithmic_bytes(R, T, H, E, K, N, n_msgs, n_sent)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or 128 * 2**20
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream(dev)
+
+    def step():
+        layer.layout(topk, out=lay, sync=False)
+        layer.dispatch(x, lay, recv)
+        layer.combine(eo, wts, topk, lay, out)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if layer.device_status() != 0:
+        raise SystemExit(f"device status {layer.device_status()} after warm-up")
+
+    clocks = ClockSampler(local)
+    time.sleep(0.6)
+    K_ = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K_)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    for i in range(K_):
+        flush.zero_()
+        e = evs[i]
+        e[0].record(st)
+        layer.layout(topk, out=lay, sync=False)
+        e[1].record(st)
+        layer.dispatch(x, lay, recv)
+        e[2].record(st)
+        layer.combine(eo, wts, topk, lay, out)
+        e[3].record(st)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    wall1 = time.time()
+    clocks.stop()
+    status = layer.device_status()
+    if status != 0:
+        raise SystemExit(f"device status {status} in the timed region")
+    t_layout = np.array([e[0].elapsed_time(e[1]) for e in evs]) * 1e-3
+    t_disp = np.array([e[1].elapsed_time(e[2]) for e in evs]) * 1e-3
+    t_comb = np.array([e[2].elapsed_time(e[3]) for e in evs]) * 1e-3
+    t_step = t_layout + t_disp + t_comb
+    step_s = float(t_step.mean())
+    if dist:
+        tt = torch.tensor([step_s], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        step_s = float(tt.item())
+    total_bytes = sum(ab.values())
+    value = world * total_bytes / step_s / 1e9
+
+    peak, peak_kind = read_peaks()
+    per_op = {"layout": float(t_layout.mean()), "dispatch": float(t_disp.mean()), "combine": float(t_comb.mean())}
+    dom = max(("dispatch", "combine"), key=lambda k: per_op[k])
+    achieved = ab[dom] / per_op[dom] / 1e9
+    roofline = {"kernel": f"{dom}_kernel", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                "peak_kind": f"{peak_kind} hbm_gbs (copy)", "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": read_traffic(dom, args.workload),
+                "algorithmic_bytes_per_launch": ab[dom],
+                "per_op": {k: {"us": round(per_op[k] * 1e6, 2), "bytes": ab[k],
+                               "GBps": round(ab[k] / per_op[k] / 1e9, 1),
+                               "frac": round(ab[k] / per_op[k] / 1e9 / peak, 4)} for k in per_op}}
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K_,
+        "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "num_tokens": T,
+                   "hidden": H, "ranks": R, "experts": E, "topk": K, "n_recv": N, "messages": n_msgs,
+                   "rows_per_msg": layer.G, "l2": "flushed between steps (write of 2x L2, outside the events)",
+                   "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "us_per_layer": round((per_op["dispatch"] + per_op["combine"]) * 1e6, 2),
+        "dispatch_us": round(per_op["dispatch"] * 1e6, 2), "combine_us": round(per_op["combine"] * 1e6, 2),
+        "layout_us": round(per_op["layout"] * 1e6, 2),
+        "roofline": roofline,
+        "gpu_launches": 3 * K_,
+        "clocks": clocks.summary(wall0, wall1),
+        "wall_s_timed_region": round(wall1 - wall0, 3),
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(layer, w, idx, wt, x, lay, recv, out, ab, dev, K_=max(3, min(K_, 10)))
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        rates, full, note = cpu_oracle_rates(w, idx, wt, x, eo)
+        v, secs = step_rate(full, rates)
+        result["cpu_baseline"] = {"value": round(v, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                  "sample": note, "per_op_GBps": {k: round(r, 3) for k, r in rates.items()}}
+    layer.close()
+    if rank == 0:
+        print(json.dumps(result))
+    if dist:
+        dist.destroy_process_group()
+
+
+def run_e2e(layer, w, idx, wt, x_dev, lay, recv, out, ab, dev, K_):
+    """The same step through the public API with host buffers: pinned host ->
+    device copies of x, topk_idx and topk_weights, layout, dispatch, identity
+    expert (combine reads the receive buffer), combine, device -> host copy of
+    the output; all inside the timed region."""
+    import torch
+    T, H, K = w.num_tokens, w.hidden, w.topk
+    x_h = x_dev.cpu().pin_memory()
+    idx_h = torch.from_numpy(idx).pin_memory()
+    wt_h = torch.from_numpy(wt).pin_memory()
+    out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(x_dev)
+    idx_d = torch.empty((T, K), dtype=torch.int32, device=dev)
+    wt_d = torch.empty((T, K), dtype=torch.float32, device=dev)
+
+    def step():
+        x_d.copy_(x_h, non_blocking=True)
+        idx_d.copy_(idx_h, non_blocking=True)
+        wt_d.copy_(wt_h, non_blocking=True)
+        layer.layout(idx_d, out=lay, sync=False)
+        layer.dispatch(x_d, lay, recv)
+        layer.combine(recv, wt_d, idx_d, lay, out)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    st = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(K_):
+        step()
+    e1.record(st)
+    torch.cuda.synchronize(dev)
+    secs = e0.elapsed_time(e1) * 1e-3 / K_
+    h2d = x_h.numel() * 2 + idx_h.numel() * 4 + wt_h.numel() * 4
+    d2h = out_h.numel() * 2
+    return {"value": round(sum(ab.values()) / secs / 1e9, 1), "unit": "GB/s", "ms_per_step": round(secs * 1e3, 3),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": K_,
+            "note": "pinned host buffers; identity expert between dispatch and combine"}
+
+
+def run_reference(args, w, world, rank):
+    """The CPU oracle, as it stands, on the host cores: each step a bounded
+    sample of the same workload; same metric and unit."""
+    if rank != 0:
+        return
+    import torch
+
+    import workloads as W
+    idx, wt = W.make_routing(w)
+    x = W.make_x_torch(w, "cpu")
+    eo_rows = None
+    import oracle
+    lay = oracle.layout(w.num_ranks, w.tokens_per_rank, w.num_experts, idx, oracle.default_rows_per_msg(w.hidden))
+    eo_rows = lay["n_recv"]
+    # expert output: only the sampled rows are read; draw it lazily by rows
+    eo = _LazyRows(eo_rows, w.hidden, w.seed)
+    vals = []
+    for i in range(args.warmup + args.steps):
+        rates, full, note = cpu_oracle_rates(w, idx, wt, x, eo, budget_s=1.0)
+        v, secs = step_rate(full, rates)
+        if i >= args.warmup:
+            vals.append((v, secs))
+    v = float(np.mean([a for a, _ in vals]))
+    secs = float(np.mean([b for _, b in vals]))
+    res = {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "GB/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic", "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload},
+           "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": note},
+           "e2e": {"value": round(v, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res))
+
+
+class _LazyRows:
+    """Expert output rows drawn on demand (row r from a seed of its own), so
+    that the CPU reference never materialises the whole [N, H] array."""
+
+    def __init__(self, rows, hidden, seed):
+        self.rows, self.hidden, self.seed = rows, hidden, seed
+        self.device = "cpu"
+
+    def index_select(self, dim, index):
+        import torch
+        out = torch.empty((len(index), self.hidden), dtype=torch.bfloat16)
+        for i, r in enumerate(index.tolist()):
+            g = torch.Generator().manual_seed(self.seed * 1000003 + r)
+            out[i] = torch.randn(self.hidden, generator=g)
+        return out
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,182 @@
+"""ctypes binding of libep.so: the C ABI of include/ep.h, same names, argument
+marshalling only.  Every step of the layer runs in the library's CUDA kernels;
+there is no other code path.  If libep.so is missing, importing this module
+raises."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libep.so")
+
+EP_OK = 0
+EP_ERR_INVALID_ARG = 1
+EP_ERR_CAPACITY = 2
+EP_ERR_TIMEOUT = 3
+EP_ERR_CUDA = 4
+EP_ERR_NOT_READY = 5
+EP_DEBUG_DISABLE_CONSUMER = 0x1
+
+_STATUS_NAMES = {0: "EP_OK", 1: "EP_ERR_INVALID_ARG", 2: "EP_ERR_CAPACITY", 3: "EP_ERR_TIMEOUT",
+                 4: "EP_ERR_CUDA", 5: "EP_ERR_NOT_READY"}
+
+
+class ep_config(ctypes.Structure):
+    _fields_ = [("num_ranks", ctypes.c_int32), ("tokens_per_rank", ctypes.c_int32),
+                ("hidden", ctypes.c_int32), ("num_experts", ctypes.c_int32), ("topk", ctypes.c_int32),
+                ("channels", ctypes.c_int32), ("ring_depth", ctypes.c_int32),
+                ("max_inflight", ctypes.c_int32), ("batch", ctypes.c_int32),
+                ("rows_per_msg", ctypes.c_int32), ("drain_batch", ctypes.c_int32),
+                ("debug_flags", ctypes.c_int32), ("timeout_ns", ctypes.c_uint64)]
+
+
+class ep_transfer_cmd(ctypes.Structure):
+    _fields_ = [("dst_rank", ctypes.c_uint32), ("size", ctypes.c_uint32), ("src_offset", ctypes.c_uint64),
+                ("dst_offset", ctypes.c_uint64), ("type", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
+
+
+class ep_layout_out(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "num_tokens_per_expert", "num_tokens_per_rank", "is_token_in_rank", "token_slot", "recv_off",
+        "send_off", "msg_count", "recv_count", "recv_base", "expert_off")]
+
+
+class ep_cmd_log(ctypes.Structure):
+    _fields_ = [("cmds", ctypes.c_void_p), ("count", ctypes.c_void_p),
+                ("capacity_per_channel", ctypes.c_int64), ("channels", ctypes.c_int32)]
+
+
+class ep_ring_stats(ctypes.Structure):
+    _fields_ = [("head", ctypes.c_uint64), ("tail", ctypes.c_uint64), ("batches", ctypes.c_uint64),
+                ("stall_polls", ctypes.c_uint64), ("max_batch", ctypes.c_uint32),
+                ("max_inflight", ctypes.c_uint32), ("last_count", ctypes.c_int64)]
+
+
+class ep_info(ctypes.Structure):
+    _fields_ = [("rows_per_msg", ctypes.c_int32), ("sm_count", ctypes.c_int32),
+                ("dispatch_grid", ctypes.c_int32), ("dispatch_stages", ctypes.c_int32),
+                ("dispatch_stage_bytes", ctypes.c_int32), ("combine_grid", ctypes.c_int32),
+                ("layout_tiles", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("log_capacity_per_channel", ctypes.c_int64), ("scratch_bytes", ctypes.c_int64)]
+
+
+assert ctypes.sizeof(ep_transfer_cmd) == 32
+assert ctypes.sizeof(ep_config) == 56
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libep.so is not built ({LIB_PATH}); run "
+                      "`python -m combine_ep_layout_04_gb300.build` (needs nvcc)")
+lib = ctypes.CDLL(LIB_PATH)
+
+_h = ctypes.c_void_p
+_p = ctypes.c_void_p
+_sigs = {
+    "ep_config_init": ([ctypes.POINTER(ep_config)] + [ctypes.c_int32] * 5, ctypes.c_int),
+    "ep_config_check": ([ctypes.POINTER(ep_config)], ctypes.c_int),
+    "ep_create": ([ctypes.POINTER(ep_config), ctypes.POINTER(_h)], ctypes.c_int),
+    "ep_destroy": ([_h], ctypes.c_int),
+    "ep_status_str": ([ctypes.c_int], ctypes.c_char_p),
+    "ep_last_device_status": ([_h, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
+    "ep_reset": ([_h], ctypes.c_int),
+    "ep_layout": ([_h, _p, ctypes.POINTER(ep_layout_out), ctypes.POINTER(ctypes.c_int64), _p], ctypes.c_int),
+    "ep_dispatch": ([_h, _p, ctypes.POINTER(ep_layout_out), _p, ctypes.c_int64, _p], ctypes.c_int),
+    "ep_combine": ([_h, _p, ctypes.c_int64, _p, _p, ctypes.POINTER(ep_layout_out), _p, _p], ctypes.c_int),
+    "ep_cmd_log_get": ([_h, ctypes.POINTER(ep_cmd_log)], ctypes.c_int),
+    "ep_ring_stats_get": ([_h, ctypes.POINTER(ep_ring_stats), ctypes.c_int32], ctypes.c_int),
+    "ep_check_completion": ([_h, ctypes.c_int32, ctypes.c_uint64], ctypes.c_int),
+    "ep_get_info": ([_h, ctypes.POINTER(ep_info)], ctypes.c_int),
+}
+for _name, (_args, _res) in _sigs.items():
+    _f = getattr(lib, _name)
+    _f.argtypes = _args
+    _f.restype = _res
+
+EXPORTED = tuple(_sigs)
+
+
+class EpError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {status_str(status)}" if what else status_str(status))
+
+
+def status_str(status: int) -> str:
+    return lib.ep_status_str(status).decode()
+
+
+def check(status: int, what: str = "") -> None:
+    if status != EP_OK:
+        raise EpError(status, what)
+
+
+# ----------------------------------------------------------------- the calls
+
+def ep_config_init(num_ranks, tokens_per_rank, hidden, num_experts, topk) -> ep_config:
+    cfg = ep_config()
+    check(lib.ep_config_init(ctypes.byref(cfg), num_ranks, tokens_per_rank, hidden, num_experts, topk),
+          "ep_config_init")
+    return cfg
+
+
+def ep_config_check(cfg: ep_config) -> int:
+    return lib.ep_config_check(ctypes.byref(cfg))
+
+
+def ep_create(cfg: ep_config) -> ctypes.c_void_p:
+    h = _h()
+    check(lib.ep_create(ctypes.byref(cfg), ctypes.byref(h)), "ep_create")
+    return h
+
+
+def ep_destroy(h) -> None:
+    check(lib.ep_destroy(h), "ep_destroy")
+
+
+def ep_last_device_status(h) -> int:
+    code = ctypes.c_int32(0)
+    check(lib.ep_last_device_status(h, ctypes.byref(code)), "ep_last_device_status")
+    return int(code.value)
+
+
+def ep_reset(h) -> None:
+    check(lib.ep_reset(h), "ep_reset")
+
+
+def ep_layout(h, topk_idx_ptr: int, out: ep_layout_out, stream: int, want_n: bool = True):
+    n = ctypes.c_int64(-1)
+    check(lib.ep_layout(h, topk_idx_ptr, ctypes.byref(out), ctypes.byref(n) if want_n else None, stream),
+          "ep_layout")
+    return int(n.value) if want_n else None
+
+
+def ep_dispatch(h, x_ptr: int, layout: ep_layout_out, recv_ptr: int, capacity_rows: int, stream: int) -> None:
+    check(lib.ep_dispatch(h, x_ptr, ctypes.byref(layout), recv_ptr, capacity_rows, stream), "ep_dispatch")
+
+
+def ep_combine(h, expert_out_ptr: int, expert_out_rows: int, weights_ptr: int, topk_idx_ptr: int,
+               layout: ep_layout_out, out_ptr: int, stream: int) -> None:
+    check(lib.ep_combine(h, expert_out_ptr, expert_out_rows, weights_ptr, topk_idx_ptr, ctypes.byref(layout),
+                         out_ptr, stream), "ep_combine")
+
+
+def ep_cmd_log_get(h) -> ep_cmd_log:
+    log = ep_cmd_log()
+    check(lib.ep_cmd_log_get(h, ctypes.byref(log)), "ep_cmd_log_get")
+    return log
+
+
+def ep_ring_stats_get(h, n: int) -> list:
+    arr = (ep_ring_stats * n)()
+    check(lib.ep_ring_stats_get(h, arr, n), "ep_ring_stats_get")
+    return [{f: getattr(a, f) for f, _ in ep_ring_stats._fields_} for a in arr]
+
+
+def ep_check_completion(h, channel: int, cmd_idx: int) -> int:
+    return lib.ep_check_completion(h, channel, cmd_idx)
+
+
+def ep_get_info(h) -> dict:
+    info = ep_info()
+    check(lib.ep_get_info(h, ctypes.byref(info)), "ep_get_info")
+    return {f: getattr(info, f) for f, _ in ep_info._fields_}

@@ -1,0 +1,309 @@
+// ep_api.cu -- host side of the libep C ABI (declared in include/ep.h):
+// configuration checks, the one device allocation a handle owns, launches,
+// status and statistics.
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "ep_internal.cuh"
+
+using ep::DevState;
+
+namespace {
+
+bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Rows per message: 8 when a bf16 row is under the 7 KB packing threshold
+// (UCCL-EP article s4.1; batch size 8 from s5.3), else 1.
+int default_rows_per_msg(int hidden) { return 2 * hidden < 7 * 1024 ? 8 : 1; }
+
+ep_status cuda_ok(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
+
+bool layout_ptrs_ok(const ep_layout_out *o) {
+    return o && o->num_tokens_per_expert && o->num_tokens_per_rank && o->is_token_in_rank && o->token_slot &&
+           o->recv_off && o->send_off && o->msg_count && o->recv_count && o->recv_base && o->expert_off;
+}
+
+// Carves one allocation into 256-byte aligned pieces.
+struct Carver {
+    size_t off = 0;
+    template <typename T>
+    size_t take(size_t count) {
+        const size_t at = (off + 255) & ~size_t(255);
+        off = at + count * sizeof(T);
+        return at;
+    }
+};
+
+}  // namespace
+
+extern "C" {
+
+ep_status ep_config_init(ep_config *cfg, int32_t num_ranks, int32_t tokens_per_rank, int32_t hidden,
+                         int32_t num_experts, int32_t topk) {
+    if (!cfg) return EP_ERR_INVALID_ARG;
+    memset(cfg, 0, sizeof(*cfg));
+    cfg->num_ranks = num_ranks;
+    cfg->tokens_per_rank = tokens_per_rank;
+    cfg->hidden = hidden;
+    cfg->num_experts = num_experts;
+    cfg->topk = topk;
+    cfg->channels = 8;        // HT_CHANNELS
+    cfg->ring_depth = 1024;   // FIFO_DEPTH
+    cfg->max_inflight = 256;  // MAX_INFLIGHT
+    cfg->batch = 8;           // up to 8 commands per batch
+    cfg->rows_per_msg = 0;    // default rule
+    cfg->drain_batch = 32;    // DRAIN_BATCH_SIZE
+    cfg->debug_flags = 0;
+    cfg->timeout_ns = ep::kDefaultTimeoutNs;
+    return EP_OK;
+}
+
+ep_status ep_config_check(const ep_config *c) {
+    if (!c) return EP_ERR_INVALID_ARG;
+    if (c->num_ranks < 1 || c->num_ranks > ep::kMaxRanks) return EP_ERR_INVALID_ARG;
+    if (c->tokens_per_rank < 1) return EP_ERR_INVALID_ARG;
+    if (c->hidden < 8 || c->hidden % 8 != 0) return EP_ERR_INVALID_ARG;
+    if (c->num_experts < c->num_ranks || c->num_experts % c->num_ranks != 0 || c->num_experts > 4096)
+        return EP_ERR_INVALID_ARG;
+    if (c->topk < 1 || c->topk > ep::kMaxTopk || c->topk > c->num_experts) return EP_ERR_INVALID_ARG;
+    if (c->channels < 1 || c->channels > ep::kMaxChannels) return EP_ERR_INVALID_ARG;
+    if (!is_pow2(c->ring_depth) || c->ring_depth < 8 || c->ring_depth > 65536) return EP_ERR_INVALID_ARG;
+    if (c->max_inflight < 8 || c->max_inflight > c->ring_depth) return EP_ERR_INVALID_ARG;
+    if (c->batch < 1 || c->batch > 8) return EP_ERR_INVALID_ARG;
+    if (c->rows_per_msg < 0 || c->rows_per_msg > (1 << 20)) return EP_ERR_INVALID_ARG;
+    if (c->drain_batch < 32 || c->drain_batch > 512 || c->drain_batch % 32 != 0) return EP_ERR_INVALID_ARG;
+    if (c->debug_flags & ~EP_DEBUG_DISABLE_CONSUMER) return EP_ERR_INVALID_ARG;
+    const int64_t T = static_cast<int64_t>(c->num_ranks) * c->tokens_per_rank;
+    const int64_t kmin = c->topk < c->num_ranks ? c->topk : c->num_ranks;
+    // receive rows are counted in int32
+    if (T * kmin >= (1ll << 31) || T * c->num_ranks >= (1ll << 40)) return EP_ERR_INVALID_ARG;
+    const int G = c->rows_per_msg ? c->rows_per_msg : default_rows_per_msg(c->hidden);
+    // a message's byte size is a uint32
+    if (static_cast<int64_t>(G) * 2 * c->hidden >= (1ll << 32)) return EP_ERR_INVALID_ARG;
+    return EP_OK;
+}
+
+const char *ep_status_str(ep_status s) {
+    switch (s) {
+        case EP_OK: return "EP_OK";
+        case EP_ERR_INVALID_ARG: return "EP_ERR_INVALID_ARG";
+        case EP_ERR_CAPACITY: return "EP_ERR_CAPACITY";
+        case EP_ERR_TIMEOUT: return "EP_ERR_TIMEOUT";
+        case EP_ERR_CUDA: return "EP_ERR_CUDA";
+        case EP_ERR_NOT_READY: return "EP_ERR_NOT_READY";
+    }
+    return "EP_ERR_UNKNOWN";
+}
+
+ep_status ep_create(const ep_config *cfg, ep_handle *out) {
+    if (!out) return EP_ERR_INVALID_ARG;
+    *out = nullptr;
+    ep_status st = ep_config_check(cfg);
+    if (st != EP_OK) return st;
+    ep_ctx *h = new (std::nothrow) ep_ctx();
+    if (!h) return EP_ERR_INVALID_ARG;
+    h->cfg = *cfg;
+    if (h->cfg.timeout_ns == 0) h->cfg.timeout_ns = ep::kDefaultTimeoutNs;
+    h->G = cfg->rows_per_msg ? cfg->rows_per_msg : default_rows_per_msg(cfg->hidden);
+    const int R = cfg->num_ranks, E = cfg->num_experts, C = cfg->channels, D = cfg->ring_depth;
+    const int64_t Tpr = cfg->tokens_per_rank, T = R * Tpr;
+    if (cudaGetDevice(&h->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+        delete h;
+        return EP_ERR_CUDA;
+    }
+    h->tiles = static_cast<int>((T + 255) / 256);
+    h->msgs_per_pair = static_cast<int>((Tpr + h->G - 1) / h->G);
+    // log capacity: every message of every (s, d) with d in the busiest channel
+    const int64_t ranks_per_chan = (R + C - 1) / C;
+    const int64_t kmin = cfg->topk < ranks_per_chan ? cfg->topk : ranks_per_chan;
+    h->log_cap = (T * kmin + h->G - 1) / h->G + static_cast<int64_t>(R) * ranks_per_chan;
+    if ((st = ep::plan_dispatch(h)) != EP_OK || (st = ep::plan_combine(h)) != EP_OK) {
+        delete h;
+        return st;
+    }
+
+    Carver cv;
+    const size_t o_err = cv.take<int32_t>(1);
+    const size_t o_ticket = cv.take<unsigned long long>(1);
+    const size_t o_done = cv.take<unsigned int>(1);
+    const size_t o_desc = cv.take<unsigned long long>(static_cast<size_t>(h->tiles) * R);
+    const size_t o_hist = cv.take<int32_t>(static_cast<size_t>(R) * E);
+    const size_t o_pref = cv.take<int32_t>(static_cast<size_t>(R + 1) * R);
+    const size_t o_nrecv = cv.take<int64_t>(1);
+    const size_t o_slots = cv.take<ep_transfer_cmd>(static_cast<size_t>(C) * D);
+    const size_t o_status = cv.take<unsigned long long>(static_cast<size_t>(C) * D);
+    const size_t o_head = cv.take<unsigned long long>(static_cast<size_t>(C) * ep::kHeadStride);
+    const size_t o_tail = cv.take<unsigned long long>(static_cast<size_t>(C) * ep::kHeadStride);
+    const size_t o_stats = cv.take<ep::RingStatsDev>(C);
+    const size_t o_log = cv.take<ep_transfer_cmd>(static_cast<size_t>(C) * h->log_cap);
+    const size_t o_lcount = cv.take<int64_t>(C);
+    const size_t n_fill = h->G > 1 ? static_cast<size_t>(R) * R * h->msgs_per_pair : 0;
+    const size_t o_fill = cv.take<unsigned int>(n_fill > 0 ? n_fill : 1);
+    h->alloc_bytes = cv.off;
+    if (cudaMalloc(&h->alloc_base, h->alloc_bytes) != cudaSuccess) {
+        delete h;
+        return EP_ERR_CUDA;
+    }
+    if (cudaMemset(h->alloc_base, 0, h->alloc_bytes) != cudaSuccess) {
+        cudaFree(h->alloc_base);
+        delete h;
+        return EP_ERR_CUDA;
+    }
+    uint8_t *b = static_cast<uint8_t *>(h->alloc_base);
+    DevState &d = h->dev;
+    d.err = reinterpret_cast<int32_t *>(b + o_err);
+    d.ticket = reinterpret_cast<unsigned long long *>(b + o_ticket);
+    d.done = reinterpret_cast<unsigned int *>(b + o_done);
+    d.tile_desc = reinterpret_cast<unsigned long long *>(b + o_desc);
+    d.hist = reinterpret_cast<int32_t *>(b + o_hist);
+    d.col_prefix = reinterpret_cast<int32_t *>(b + o_pref);
+    d.n_recv = reinterpret_cast<int64_t *>(b + o_nrecv);
+    d.slots = reinterpret_cast<ep_transfer_cmd *>(b + o_slots);
+    d.status = reinterpret_cast<unsigned long long *>(b + o_status);
+    d.head = reinterpret_cast<unsigned long long *>(b + o_head);
+    d.tail = reinterpret_cast<unsigned long long *>(b + o_tail);
+    d.stats = reinterpret_cast<ep::RingStatsDev *>(b + o_stats);
+    d.log = reinterpret_cast<ep_transfer_cmd *>(b + o_log);
+    d.log_count = reinterpret_cast<int64_t *>(b + o_lcount);
+    d.msg_fill = n_fill > 0 ? reinterpret_cast<unsigned int *>(b + o_fill) : nullptr;
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaFree(h->alloc_base);
+        delete h;
+        return EP_ERR_CUDA;
+    }
+    *out = h;
+    return EP_OK;
+}
+
+ep_status ep_destroy(ep_handle h) {
+    if (!h) return EP_ERR_INVALID_ARG;
+    const cudaError_t e1 = cudaDeviceSynchronize();
+    const cudaError_t e2 = cudaFree(h->alloc_base);
+    delete h;
+    return (e1 == cudaSuccess && e2 == cudaSuccess) ? EP_OK : EP_ERR_CUDA;
+}
+
+ep_status ep_last_device_status(ep_handle h, int32_t *code) {
+    if (!h || !code) return EP_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return EP_ERR_CUDA;
+    return cuda_ok(cudaMemcpy(code, h->dev.err, sizeof(int32_t), cudaMemcpyDeviceToHost));
+}
+
+ep_status ep_reset(ep_handle h) {
+    if (!h) return EP_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return EP_ERR_CUDA;
+    if (cudaMemset(h->alloc_base, 0, h->alloc_bytes) != cudaSuccess) return EP_ERR_CUDA;
+    return cuda_ok(cudaDeviceSynchronize());
+}
+
+ep_status ep_layout(ep_handle h, const int32_t *topk_idx, const ep_layout_out *out, int64_t *n_recv_host,
+                    void *stream) {
+    if (!h || !topk_idx || !layout_ptrs_ok(out)) return EP_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    ep_status s = ep::launch_layout(h, topk_idx, out, st);
+    if (s != EP_OK || !n_recv_host) return s;
+    int64_t n = 0;
+    if (cudaMemcpyAsync(&n, h->dev.n_recv, sizeof(n), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return EP_ERR_CUDA;
+    *n_recv_host = n;
+    return EP_OK;
+}
+
+ep_status ep_dispatch(ep_handle h, const void *x, const ep_layout_out *layout, void *recv,
+                      int64_t recv_capacity_rows, void *stream) {
+    if (!h || !x || !recv || !layout_ptrs_ok(layout) || recv_capacity_rows < 0) return EP_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(recv)) return EP_ERR_INVALID_ARG;
+    return ep::launch_dispatch(h, x, layout, recv, recv_capacity_rows, static_cast<cudaStream_t>(stream));
+}
+
+ep_status ep_combine(ep_handle h, const void *expert_out, int64_t expert_out_rows, const float *topk_weights,
+                     const int32_t *topk_idx, const ep_layout_out *layout, void *out, void *stream) {
+    if (!h || !expert_out || !topk_weights || !topk_idx || !layout_ptrs_ok(layout) || !out || expert_out_rows < 0)
+        return EP_ERR_INVALID_ARG;
+    if (!aligned16(expert_out) || !aligned16(out)) return EP_ERR_INVALID_ARG;
+    return ep::launch_combine(h, expert_out, expert_out_rows, topk_weights, topk_idx, layout, out,
+                              static_cast<cudaStream_t>(stream));
+}
+
+ep_status ep_cmd_log_get(ep_handle h, ep_cmd_log *out) {
+    if (!h || !out) return EP_ERR_INVALID_ARG;
+    out->cmds = h->dev.log;
+    out->count = h->dev.log_count;
+    out->capacity_per_channel = h->log_cap;
+    out->channels = h->cfg.channels;
+    return EP_OK;
+}
+
+ep_status ep_ring_stats_get(ep_handle h, ep_ring_stats *out, int32_t n) {
+    if (!h || !out || n < 0 || n > h->cfg.channels) return EP_ERR_INVALID_ARG;
+    if (n == 0) return EP_OK;
+    if (cudaDeviceSynchronize() != cudaSuccess) return EP_ERR_CUDA;
+    const int C = h->cfg.channels;
+    ep::RingStatsDev *st = static_cast<ep::RingStatsDev *>(malloc(sizeof(ep::RingStatsDev) * C));
+    unsigned long long *hd = static_cast<unsigned long long *>(malloc(sizeof(unsigned long long) * C * ep::kHeadStride));
+    unsigned long long *tl = static_cast<unsigned long long *>(malloc(sizeof(unsigned long long) * C * ep::kHeadStride));
+    int64_t *lc = static_cast<int64_t *>(malloc(sizeof(int64_t) * C));
+    ep_status rc = EP_OK;
+    if (!st || !hd || !tl || !lc) rc = EP_ERR_INVALID_ARG;
+    if (rc == EP_OK &&
+        (cudaMemcpy(st, h->dev.stats, sizeof(ep::RingStatsDev) * C, cudaMemcpyDeviceToHost) != cudaSuccess ||
+         cudaMemcpy(hd, h->dev.head, sizeof(unsigned long long) * C * ep::kHeadStride, cudaMemcpyDeviceToHost) !=
+             cudaSuccess ||
+         cudaMemcpy(tl, h->dev.tail, sizeof(unsigned long long) * C * ep::kHeadStride, cudaMemcpyDeviceToHost) !=
+             cudaSuccess ||
+         cudaMemcpy(lc, h->dev.log_count, sizeof(int64_t) * C, cudaMemcpyDeviceToHost) != cudaSuccess))
+        rc = EP_ERR_CUDA;
+    if (rc == EP_OK) {
+        for (int c = 0; c < n; ++c) {
+            out[c].head = hd[c * ep::kHeadStride];
+            out[c].tail = tl[c * ep::kHeadStride];
+            out[c].batches = st[c].batches;
+            out[c].stall_polls = st[c].stall_polls;
+            out[c].max_batch = st[c].max_batch;
+            out[c].max_inflight = st[c].max_inflight;
+            out[c].last_count = lc[c];
+        }
+    }
+    free(st);
+    free(hd);
+    free(tl);
+    free(lc);
+    return rc;
+}
+
+ep_status ep_check_completion(ep_handle h, int32_t channel, uint64_t cmd_idx) {
+    if (!h || channel < 0 || channel >= h->cfg.channels) return EP_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return EP_ERR_CUDA;
+    unsigned long long tail = 0, status = 0;
+    const size_t sidx = static_cast<size_t>(channel) * h->cfg.ring_depth + (cmd_idx & (h->cfg.ring_depth - 1));
+    if (cudaMemcpy(&tail, h->dev.tail + static_cast<size_t>(channel) * ep::kHeadStride, sizeof(tail),
+                   cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(&status, h->dev.status + sidx, sizeof(status), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return EP_ERR_CUDA;
+    // retired: the slot still holds this command marked COMPLETED, or the tail
+    // has moved past it
+    if (status == 2ull * cmd_idx + 2ull || tail > cmd_idx) return EP_OK;
+    return EP_ERR_NOT_READY;
+}
+
+ep_status ep_get_info(ep_handle h, ep_info *out) {
+    if (!h || !out) return EP_ERR_INVALID_ARG;
+    memset(out, 0, sizeof(*out));
+    out->rows_per_msg = h->G;
+    out->sm_count = h->sm_count;
+    out->dispatch_grid = h->disp_grid;
+    out->dispatch_stages = h->stages;
+    out->dispatch_stage_bytes = h->stage_bytes;
+    out->combine_grid = h->comb_grid;
+    out->layout_tiles = h->tiles;
+    out->log_capacity_per_channel = h->log_cap;
+    out->scratch_bytes = static_cast<int64_t>(h->alloc_bytes);
+    return EP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,273 @@
+// ep_internal.cuh -- shared pieces of the libep CUDA sources (sm_103a):
+// the handle, the device state it owns, the launch parameter blocks, and
+// thin inline-PTX wrappers (acquire/release accesses, %globaltimer, mbarrier,
+// 1-D TMA bulk copies).  Host-visible API: include/ep.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ep.h"
+
+namespace ep {
+
+// Limits the kernels are written for (also checked by ep_config_check).
+constexpr int kMaxRanks = 64;
+constexpr int kMaxTopk = 32;
+constexpr int kMaxChannels = 64;
+constexpr int kChunkTokens = 32;         // dispatch: tokens per chunk (one per lane)
+constexpr int kHeadStride = 16;          // u64s between two channels' head/tail words (128 B)
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+// ---------------------------------------------------------------- device state
+
+// Per-channel producer statistics (cumulative).  Matches the leading fields
+// of ep_ring_stats; head/tail/last_count are stored elsewhere.
+struct RingStatsDev {
+    unsigned long long batches;
+    unsigned long long stall_polls;
+    unsigned int max_batch;
+    unsigned int max_inflight;
+};
+
+// Device pointers the handle owns (one cudaMalloc, carved).
+struct DevState {
+    int32_t *err;                       // sticky error word (ep_status)
+    // layout scan
+    unsigned long long *ticket;         // tiles handed out so far (all calls)
+    unsigned int *done;                 // tiles finished in the current call
+    unsigned long long *tile_desc;      // [tiles * R] packed (epoch, flag, value)
+    int32_t *hist;                      // [R * E] per-call histogram scratch, left zeroed
+    int32_t *col_prefix;                // [(R + 1) * R] column prefix at each rank's first token
+    int64_t *n_recv;                    // N of the last layout
+    // rings
+    ep_transfer_cmd *slots;             // [C * D]
+    unsigned long long *status;         // [C * D] 2*idx+1 posted, 2*idx+2 retired
+    unsigned long long *head;           // [C * kHeadStride]
+    unsigned long long *tail;           // [C * kHeadStride]
+    RingStatsDev *stats;                // [C]
+    ep_transfer_cmd *log;               // [C * log_cap]
+    int64_t *log_count;                 // [C]
+    unsigned int *msg_fill;             // [R * R * msgs_per_pair] rows landed per message (G > 1)
+};
+
+// Layout kernel parameters.
+struct LayoutParams {
+    const int32_t *topk_idx;
+    ep_layout_out out;
+    DevState dev;
+    int64_t T;
+    int R, Tpr, E, K, Er, G;
+    int tiles;
+    int in_rank_vec;   // bytes per is_token_in_rank store: 16, 4 or 1
+};
+
+// Dispatch kernel parameters.
+struct DispatchParams {
+    const uint8_t *x;
+    uint8_t *recv;
+    int64_t cap_rows;
+    const int32_t *token_slot, *recv_base, *recv_count, *recv_off, *send_off, *cnt, *msg_count;
+    DevState dev;
+    int64_t T;
+    int64_t row_bytes;
+    int64_t log_cap;
+    uint64_t timeout_ns;
+    int R, Tpr, C, D, max_inflight, batch, G, drain_batch, debug;
+    int chunks_per_rank, nchunks;
+    int rows_per_item;   // tokens per item when a row fits a stage, else 1
+    int pieces;          // pieces per row when it does not, else 1
+    int piece_bytes;     // bytes per piece (a multiple of 16)
+    int stage_bytes;     // bytes per shared-memory stage
+    int stages, prefetch, meta_slots;
+    int msgs_per_pair;   // ceil(Tpr / G)
+    int slot_vec;        // 1: token_slot rows are 16-byte aligned (int4 loads)
+};
+
+// Combine kernel parameters.
+struct CombineParams {
+    const uint8_t *expert_out;
+    int64_t eo_rows;
+    const float *w;
+    const int32_t *topk_idx, *token_slot, *recv_base;
+    uint8_t *out;
+    DevState dev;
+    int64_t T;
+    int64_t row_bytes;
+    int R, K, E, Er;
+    int nseg;            // 16-byte segments per row
+};
+
+}  // namespace ep
+
+// The opaque handle of the C ABI.
+struct ep_ctx {
+    ep_config cfg;
+    int G;
+    int device;
+    int sm_count;
+    ep::DevState dev;
+    void *alloc_base;
+    size_t alloc_bytes;
+    int tiles;
+    // dispatch geometry
+    int disp_grid, disp_threads;
+    size_t disp_smem;
+    int stage_bytes, stages, prefetch, meta_slots;
+    int rows_per_item, pieces, piece_bytes;
+    int chunks_per_rank, nchunks, msgs_per_pair;
+    int64_t log_cap;
+    // combine geometry
+    int comb_grid, comb_threads;
+};
+
+namespace ep {
+
+// Host launchers (one per kernel source file).
+ep_status launch_layout(ep_ctx *h, const int32_t *topk_idx, const ep_layout_out *out,
+                        cudaStream_t st);
+ep_status launch_dispatch(ep_ctx *h, const void *x, const ep_layout_out *lay, void *recv,
+                          int64_t cap_rows, cudaStream_t st);
+ep_status launch_combine(ep_ctx *h, const void *expert_out, int64_t eo_rows, const float *w,
+                         const int32_t *topk_idx, const ep_layout_out *lay, void *out,
+                         cudaStream_t st);
+// Dispatch geometry, decided once per handle.
+ep_status plan_dispatch(ep_ctx *h);
+ep_status plan_combine(ep_ctx *h);
+
+// ------------------------------------------------------------ device helpers
+#ifdef __CUDACC__
+
+__device__ __forceinline__ void set_error(int32_t *err, int code) {
+    atomicCAS(reinterpret_cast<int *>(err), 0, code);
+}
+__device__ __forceinline__ int read_error(const int32_t *err) {
+    return *reinterpret_cast<const volatile int *>(err);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// ---- mbarrier (shared::cta)
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+// Non-blocking test of phase `parity` (true once that phase has completed).
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Potentially blocking (for a hardware-bounded time) wait on phase `parity`.
+__device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait: true when the phase completed; false when the time limit ran
+// out or (err != nullptr) another thread of the grid already raised an error.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, const int32_t *err,
+                                                  uint64_t timeout_ns) {
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try(bar, parity)) return true;
+        if (err != nullptr && read_error(err) != 0) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+}
+
+// ---- 1-D TMA bulk copies (cp.async.bulk): 16-byte aligned addresses, sizes
+// a multiple of 16.  Global -> shared completes on an mbarrier; shared ->
+// global completes per bulk async-group of the issuing thread.
+__device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gmem_src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_s2g(void *gmem_dst, const void *smem_src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gmem_dst),
+                 "r"(smem_u32(smem_src)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+// Runtime-N wait on this thread's bulk groups (N clamped to 0..15).
+__device__ __forceinline__ void bulk_wait_n(int n) {
+    switch (n) {
+        case 0: bulk_wait<0>(); break;
+        case 1: bulk_wait<1>(); break;
+        case 2: bulk_wait<2>(); break;
+        case 3: bulk_wait<3>(); break;
+        case 4: bulk_wait<4>(); break;
+        case 5: bulk_wait<5>(); break;
+        case 6: bulk_wait<6>(); break;
+        case 7: bulk_wait<7>(); break;
+        case 8: bulk_wait<8>(); break;
+        case 9: bulk_wait<9>(); break;
+        case 10: bulk_wait<10>(); break;
+        case 11: bulk_wait<11>(); break;
+        case 12: bulk_wait<12>(); break;
+        case 13: bulk_wait<13>(); break;
+        case 14: bulk_wait<14>(); break;
+        default: bulk_wait<15>(); break;
+    }
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+#endif  // __CUDACC__
+
+}  // namespace ep

@@ -1,0 +1,313 @@
+// ep_layout.cu -- token layout of one EP layer in a single pass (sm_103a).
+//
+// What it computes (the token-level routing bookkeeping of EP dispatch; UCCL-EP
+// article s1 "fine-grained token-level communication"; a layout/rank mismatch
+// is a named EP failure class in the GPU communication notes' software-stack
+// table):
+//   num_tokens_per_expert[s][e], is_token_in_rank[t][d], token_slot[t][d] =
+//   #{t' < t : in_rank[t'][d]}, and the small scans recv_off, send_off,
+//   msg_count, recv_count, recv_base, expert_off (definitions in include/ep.h).
+//
+// How: one CTA per tile of 256 tokens (one token per thread), tiles handed out
+// in launch order by a ticket counter so every tile's predecessors are
+// already running.  Per tile:
+//   1. read the K picks of each token; per-token rank mask; a histogram of
+//      picks per (source rank, expert) in shared memory (or, when the tile
+//      spans too many ranks, warp-aggregated global atomics via match_any);
+//   2. per destination column d: a warp ballot gives each token's position
+//      among the warp's members of d; warp totals give the tile aggregate;
+//   3. decoupled look-back (Merrill & Garland, "Single-pass Parallel Prefix
+//      Scan with Decoupled Look-back", 2016), one thread per column: publish
+//      the aggregate, walk back over predecessors' aggregates until an
+//      inclusive prefix is found, publish the inclusive prefix.  A descriptor
+//      is one 64-bit word {epoch:30 | flag:2 | value:32}; the epoch is derived
+//      from the ticket, so stale words from earlier calls are never taken and
+//      nothing has to be reset between calls (CUDA-graph safe);
+//   4. write token_slot (lane = column, coalesced) and, at each source rank's
+//      first token, the column prefix, from which the last tile derives the
+//      per-(s, d) counts and all the small scans.
+#include "ep_internal.cuh"
+
+namespace ep {
+namespace {
+
+constexpr int kTile = 256;
+constexpr int kWarps = kTile / 32;
+constexpr int kHistCap = 4096;             // shared-memory histogram bins
+constexpr unsigned kFull = 0xffffffffu;
+constexpr uint32_t kFlagAggregate = 1, kFlagPrefix = 2;
+
+__device__ __forceinline__ unsigned long long pack_desc(uint32_t epoch, uint32_t flag, uint32_t value) {
+    return (static_cast<unsigned long long>(epoch) << 34) | (static_cast<unsigned long long>(flag) << 32) | value;
+}
+
+// Exclusive scan of s[0, n) in place by the whole block (blockDim == kTile).
+// Returns the total.  `tmp` holds kTile + 1 ints.
+__device__ int block_excl_scan(int *s, int n, int *tmp) {
+    const int tid = threadIdx.x;
+    const int per = (n + kTile - 1) / kTile;
+    const int b = tid * per, e = min(n, b + per);
+    int local = 0;
+    for (int i = b; i < e; ++i) local += s[i];
+    tmp[tid] = local;
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int i = 0; i < kTile; ++i) {
+            int v = tmp[i];
+            tmp[i] = run;
+            run += v;
+        }
+        tmp[kTile] = run;
+    }
+    __syncthreads();
+    int run = tmp[tid];
+    for (int i = b; i < e; ++i) {
+        int v = s[i];
+        s[i] = run;
+        run += v;
+    }
+    __syncthreads();
+    return tmp[kTile];
+}
+
+// The last tile to finish: counts and small scans from the column prefixes
+// and the histogram scratch; leaves the scratch zeroed for the next call.
+__device__ void finish_layout(const LayoutParams &p, int *s_work, int *s_tmp) {
+    const int tid = threadIdx.x;
+    const int R = p.R, E = p.E, G = p.G;
+    const int32_t *P = p.dev.col_prefix;
+    // per-(s, d) counts, window offsets, message counts
+    for (int i = tid; i < R * R; i += kTile) {
+        const int s = i / R, d = i - s * R;
+        const int a = __ldcg(P + s * R + d);
+        const int c = __ldcg(P + (s + 1) * R + d) - a;
+        p.out.num_tokens_per_rank[i] = c;
+        p.out.recv_off[i] = a;
+        p.out.msg_count[i] = (c + G - 1) / G;
+        s_work[i] = c;
+    }
+    __syncthreads();
+    block_excl_scan(s_work, R * R, s_tmp);   // row-major send order
+    for (int i = tid; i < R * R; i += kTile) p.out.send_off[i] = s_work[i];
+    __syncthreads();
+    if (tid == 0) {
+        int64_t run = 0;
+        for (int d = 0; d < R; ++d) {
+            const int c = __ldcg(P + R * R + d);
+            p.out.recv_count[d] = c;
+            p.out.recv_base[d] = static_cast<int32_t>(run);
+            run += c;
+        }
+        *p.dev.n_recv = run;
+    }
+    // expert totals: copy the histogram out, clear the scratch
+    for (int e = tid; e < E; e += kTile) s_work[e] = 0;
+    __syncthreads();
+    for (int i = tid; i < R * E; i += kTile) {
+        const int v = __ldcg(p.dev.hist + i);
+        p.out.num_tokens_per_expert[i] = v;
+        p.dev.hist[i] = 0;
+        atomicAdd(&s_work[i % E], v);
+    }
+    __syncthreads();
+    block_excl_scan(s_work, E, s_tmp);
+    for (int e = tid; e < E; e += kTile) p.out.expert_off[e] = s_work[e];
+    if (tid == 0) *p.dev.done = 0u;
+}
+
+__global__ void __launch_bounds__(kTile) layout_kernel(const LayoutParams p) {
+    __shared__ int s_wcnt[kWarps][kMaxRanks];
+    __shared__ int s_excl[kMaxRanks];
+    __shared__ int s_agg[kMaxRanks];
+    __shared__ int s_hist[kHistCap];
+    __shared__ int s_tmp[kTile + 1];
+    __shared__ unsigned long long s_ticket;
+    __shared__ int s_is_last;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int R = p.R, E = p.E, K = p.K, Er = p.Er, Tpr = p.Tpr;
+
+    if (tid == 0) s_ticket = atomicAdd(p.dev.ticket, 1ull);
+    __syncthreads();
+    const unsigned long long ticket = s_ticket;
+    const int tile = static_cast<int>(ticket % static_cast<unsigned long long>(p.tiles));
+    const uint32_t epoch = static_cast<uint32_t>((ticket / p.tiles) % ((1u << 30) - 1u)) + 1u;
+
+    const int64_t t0 = static_cast<int64_t>(tile) * kTile;
+    const int nt = static_cast<int>(min(static_cast<int64_t>(kTile), p.T - t0));
+    const int s_first = static_cast<int>(t0 / Tpr);
+    const int s_last = static_cast<int>((t0 + nt - 1) / Tpr);
+    const int span = s_last - s_first + 1;
+    const bool smem_hist = span * E <= kHistCap;
+    if (smem_hist)
+        for (int i = tid; i < span * E; i += kTile) s_hist[i] = 0;
+    __syncthreads();
+
+    // 1. picks -> rank mask and histogram
+    const int64_t t = t0 + tid;
+    const bool valid = tid < nt;
+    const int s_tok = valid ? static_cast<int>(t / Tpr) : 0;
+    unsigned long long mask = 0ull;
+    for (int k = 0; k < K; ++k) {
+        int e = valid ? __ldg(p.topk_idx + t * K + k) : -1;
+        if (e < -1 || e >= E) {
+            set_error(p.dev.err, EP_ERR_INVALID_ARG);
+            e = -1;
+        }
+        if (e >= 0) mask |= 1ull << (e / Er);
+        if (smem_hist) {
+            if (e >= 0) atomicAdd(&s_hist[(s_tok - s_first) * E + e], 1);
+        } else {
+            const int key = e >= 0 ? s_tok * E + e : -1;
+            const unsigned peers = __match_any_sync(kFull, key);
+            if (key >= 0 && lane == __ffs(peers) - 1) atomicAdd(p.dev.hist + key, __popc(peers));
+        }
+    }
+
+    // is_token_in_rank row of this token
+    if (valid) {
+        uint8_t *row = p.out.is_token_in_rank + t * R;
+        if (p.in_rank_vec == 16) {
+            for (int d = 0; d < R; d += 16) {
+                uint32_t w[4];
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t v = 0;
+                    for (int b = 0; b < 4; ++b) v |= static_cast<uint32_t>((mask >> (d + 4 * q + b)) & 1ull) << (8 * b);
+                    w[q] = v;
+                }
+                *reinterpret_cast<uint4 *>(row + d) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        } else if (p.in_rank_vec == 4) {
+            for (int d = 0; d < R; d += 4) {
+                uint32_t v = 0;
+                for (int b = 0; b < 4; ++b) v |= static_cast<uint32_t>((mask >> (d + b)) & 1ull) << (8 * b);
+                *reinterpret_cast<uint32_t *>(row + d) = v;
+            }
+        } else {
+            for (int d = 0; d < R; ++d) row[d] = static_cast<uint8_t>((mask >> d) & 1ull);
+        }
+    }
+
+    // 2. per-column ballots: lane j of each 32-column group keeps column j's bits
+    const int ngroups = (R + 31) / 32;
+    unsigned colbits[kMaxRanks / 32];
+#pragma unroll
+    for (int g = 0; g < kMaxRanks / 32; ++g) {
+        colbits[g] = 0u;
+        if (g < ngroups) {
+            const int ncol = min(32, R - g * 32);
+            for (int j = 0; j < ncol; ++j) {
+                const unsigned b = __ballot_sync(kFull, (mask >> (g * 32 + j)) & 1ull);
+                if (lane == j) colbits[g] = b;
+            }
+            const int d = g * 32 + lane;
+            if (d < R) s_wcnt[warp][d] = __popc(colbits[g]);
+        }
+    }
+    __syncthreads();
+    if (tid < R) {
+        int run = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            const int v = s_wcnt[w][tid];
+            s_wcnt[w][tid] = run;
+            run += v;
+        }
+        s_agg[tid] = run;
+    }
+    __syncthreads();
+
+    // 3. decoupled look-back, one thread per column
+    if (tid < R) {
+        const int d = tid;
+        const int agg = s_agg[d];
+        unsigned long long *mine = p.dev.tile_desc + static_cast<int64_t>(tile) * R + d;
+        int excl = 0;
+        if (tile == 0) {
+            st_relaxed(mine, pack_desc(epoch, kFlagPrefix, static_cast<uint32_t>(agg)));
+        } else {
+            st_relaxed(mine, pack_desc(epoch, kFlagAggregate, static_cast<uint32_t>(agg)));
+            int pred = tile - 1;
+            const uint64_t t_start = globaltimer_ns();
+            uint32_t spins = 0;
+            while (pred >= 0) {
+                const unsigned long long v = ld_relaxed(p.dev.tile_desc + static_cast<int64_t>(pred) * R + d);
+                const uint32_t ep_v = static_cast<uint32_t>(v >> 34);
+                const uint32_t flag = static_cast<uint32_t>(v >> 32) & 3u;
+                if (ep_v == epoch && flag != 0u) {
+                    excl += static_cast<int>(static_cast<uint32_t>(v));
+                    if (flag == kFlagPrefix) break;
+                    --pred;
+                    continue;
+                }
+                if ((++spins & 63u) == 0u) {
+                    if (globaltimer_ns() - t_start > kDefaultTimeoutNs) {
+                        set_error(p.dev.err, EP_ERR_TIMEOUT);
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+            }
+            st_relaxed(mine, pack_desc(epoch, kFlagPrefix, static_cast<uint32_t>(excl + agg)));
+        }
+        s_excl[d] = excl;
+        if (tile == p.tiles - 1) p.dev.col_prefix[R * R + d] = excl + agg;
+    }
+    __syncthreads();
+
+    // 4. token_slot, lane = column; column prefix at each rank's first token
+#pragma unroll
+    for (int g = 0; g < kMaxRanks / 32; ++g) {
+        const int d = g * 32 + lane;
+        if (g >= ngroups || d >= R) continue;
+        const unsigned bits = colbits[g];
+        const int base = s_excl[d] + s_wcnt[warp][d];
+        for (int j = 0; j < 32; ++j) {
+            const int local = warp * 32 + j;
+            if (local >= nt) break;
+            const int64_t tt = t0 + local;
+            const int pre = base + __popc(bits & ((1u << j) - 1u));
+            p.out.token_slot[tt * R + d] = ((bits >> j) & 1u) ? pre : -1;
+            if (tt % Tpr == 0) p.dev.col_prefix[static_cast<int64_t>(tt / Tpr) * R + d] = pre;
+        }
+    }
+    if (smem_hist) {
+        __syncthreads();
+        for (int i = tid; i < span * E; i += kTile) {
+            const int v = s_hist[i];
+            if (v) atomicAdd(p.dev.hist + static_cast<int64_t>(s_first) * E + i, v);
+        }
+    }
+
+    // 5. the last tile to finish derives the small scans
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_is_last = (atomicAdd(p.dev.done, 1u) == static_cast<unsigned>(p.tiles - 1));
+    __syncthreads();
+    if (!s_is_last) return;
+    __threadfence();
+    finish_layout(p, s_hist, s_tmp);
+}
+
+}  // namespace
+
+ep_status launch_layout(ep_ctx *h, const int32_t *topk_idx, const ep_layout_out *out, cudaStream_t st) {
+    LayoutParams p{};
+    p.topk_idx = topk_idx;
+    p.out = *out;
+    p.dev = h->dev;
+    p.R = h->cfg.num_ranks;
+    p.Tpr = h->cfg.tokens_per_rank;
+    p.T = static_cast<int64_t>(p.R) * p.Tpr;
+    p.E = h->cfg.num_experts;
+    p.K = h->cfg.topk;
+    p.Er = p.E / p.R;
+    p.G = h->G;
+    p.tiles = h->tiles;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(out->is_token_in_rank);
+    p.in_rank_vec = (p.R % 16 == 0 && a % 16 == 0) ? 16 : (p.R % 4 == 0 && a % 4 == 0) ? 4 : 1;
+    layout_kernel<<<h->tiles, kTile, 0, st>>>(p);
+    return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+}  // namespace ep

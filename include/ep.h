@@ -1,0 +1,249 @@
+/*
+ * ep.h -- C ABI of libep: token layout, dispatch and combine of one MoE
+ * expert-parallel (EP) layer on one GB300 GPU, with the EP group's R ranks
+ * held as partitions of device buffers.
+ *
+ * Articles this interface follows:
+ *  [UCCL-EP] "UCCL-EP: GPU-side FIFO queues and CPU proxy threads"
+ *            (peacm.com/news/835744)
+ *  [GIN]     "NCCL GIN: device-initiated GPU networking" (bjdmk.com.cn/news/2086017)
+ *  [NOTES]   "GPU communication mechanisms and optimisation techniques"
+ *            (blog.zhenwei.site)
+ *
+ * Conventions for every call:
+ *  - All tensor arguments are DEVICE pointers owned by the caller (e.g. torch
+ *    allocations); the library never frees them.  Row-major, dense.
+ *  - bf16 tensors are passed as void* holding IEEE bfloat16 bits.
+ *  - Device pointers of row data (x, recv, expert_out, out) must be 16-byte
+ *    aligned; hidden must be a multiple of 8 (rows are whole 16-byte units).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Work is enqueued on it and the call returns without waiting, except where
+ *    a call says it synchronises.
+ *  - Every call returns an ep_status.  Arguments are checked on the host before
+ *    anything is launched (EP_ERR_INVALID_ARG).  Errors found on the device
+ *    (a pick outside [-1, E), a receive buffer too small, a bounded wait that
+ *    ran out) set a sticky per-handle error word; the kernels then stop early
+ *    and never trap.  Read it with ep_last_device_status; clear it (and the
+ *    ring state) with ep_reset.
+ *  - A handle is used by one host thread at a time; calls on one handle must
+ *    be ordered on one stream (they share the handle's rings and scratch).
+ */
+#ifndef EP_H_
+#define EP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes.  EP_ERR_CAPACITY is the analogue of GIN_ERR_WINDOW_FULL and
+ * EP_ERR_NOT_READY of GIN_ERR_SIGNAL_PENDING ([GIN] s4.2.1 error codes). */
+typedef enum {
+    EP_OK = 0,
+    EP_ERR_INVALID_ARG = 1,
+    EP_ERR_CAPACITY = 2,
+    EP_ERR_TIMEOUT = 3,
+    EP_ERR_CUDA = 4,
+    EP_ERR_NOT_READY = 5
+} ep_status;
+
+typedef struct ep_ctx *ep_handle;
+
+/* Layer shape and ring settings.  Defaults (ep_config_init) are the
+ * [UCCL-EP] s5.2 tuning table: 8 channels (HT_CHANNELS), ring depth 1024
+ * (FIFO_DEPTH), 256 commands in flight per channel (MAX_INFLIGHT), consumer
+ * poll batch 32 (DRAIN_BATCH_SIZE); batches of up to 8 commands (s2.2); rows
+ * per message 8 when a row is under 7 KB, else 1 (s4.1, s5.3). */
+typedef struct {
+    int32_t num_ranks;       /* R, 1..64 */
+    int32_t tokens_per_rank; /* Tpr >= 1; T = R * Tpr tokens, source rank of t is t / Tpr */
+    int32_t hidden;          /* H, multiple of 8; a row is 2*H bytes of bf16 */
+    int32_t num_experts;     /* E, a multiple of R; expert e lives on rank e / (E/R) */
+    int32_t topk;            /* K, 1..32 */
+    int32_t channels;        /* C, 1..64: rings; a message to rank d goes to ring d % C */
+    int32_t ring_depth;      /* D, power of two, 8..65536 slots per ring */
+    int32_t max_inflight;    /* 8..D: producers wait while head - tail would exceed it */
+    int32_t batch;           /* 1..8 commands reserved per head update */
+    int32_t rows_per_msg;    /* G >= 1 rows per TransferCmd message; 0 = default rule */
+    int32_t drain_batch;     /* 32 or a multiple of it: slots a consumer polls per step */
+    int32_t debug_flags;     /* EP_DEBUG_* bits; 0 in normal use */
+    uint64_t timeout_ns;     /* limit of every device-side wait; 0 = 2 s */
+} ep_config;
+
+/* Test hook: ring consumers do not run, so producers see a full ring and their
+ * bounded flow-control wait ends in EP_ERR_TIMEOUT (no GPU hang, no trap). */
+#define EP_DEBUG_DISABLE_CONSUMER 0x1
+
+/* One ring record ([UCCL-EP] s2.3 TransferCmd; WRITE only), 32 bytes.
+ *  dst_rank:   destination rank d.
+ *  size:       payload bytes = rows * 2 * hidden.
+ *  src_offset: byte offset into the logical send buffer, whose rows are
+ *              ordered (source rank, destination rank, row) -- send_off.
+ *  dst_offset: byte offset into rank d's receive window, i.e. relative to
+ *              recv row recv_base[d] ([GIN] s2.2.1 byte-offset windows).
+ *  type:       0 = WRITE.  reserved: 0. */
+typedef struct {
+    uint32_t dst_rank;
+    uint32_t size;
+    uint64_t src_offset;
+    uint64_t dst_offset;
+    uint32_t type;
+    uint32_t reserved;
+} ep_transfer_cmd;
+
+/* Caller-owned device outputs of ep_layout (inputs of dispatch / combine).
+ * Shapes use R ranks, T tokens, E experts; all int32 except is_token_in_rank.
+ *  num_tokens_per_expert [R, E]: picks of rank s's tokens that name expert e
+ *  num_tokens_per_rank   [R, R]: cnt[s][d] = tokens of rank s that reach rank d
+ *  is_token_in_rank      [T, R] uint8: 1 if some pick of t lives on rank d
+ *  token_slot            [T, R]: row of (t, d) inside rank d's window, or -1
+ *  recv_off              [R, R]: first window row of source s in window d
+ *  send_off              [R, R]: row-major exclusive scan of cnt
+ *  msg_count             [R, R]: ceil(cnt / G)
+ *  recv_count            [R]:    rows received by rank d
+ *  recv_base             [R]:    exclusive scan of recv_count (window starts)
+ *  expert_off            [E]:    exclusive scan over e of total picks of e */
+typedef struct {
+    int32_t *num_tokens_per_expert;
+    int32_t *num_tokens_per_rank;
+    uint8_t *is_token_in_rank;
+    int32_t *token_slot;
+    int32_t *recv_off;
+    int32_t *send_off;
+    int32_t *msg_count;
+    int32_t *recv_count;
+    int32_t *recv_base;
+    int32_t *expert_off;
+} ep_layout_out;
+
+/* Library-owned view of the per-channel TransferCmd logs written by the ring
+ * consumers during the last ep_dispatch.  Device pointers, valid until
+ * ep_destroy; channel c's records are cmds[c * capacity_per_channel + i]
+ * for i < count[c] (count is a device array of int64, written at the end of
+ * each dispatch). */
+typedef struct {
+    ep_transfer_cmd *cmds;
+    int64_t *count;
+    int64_t capacity_per_channel;
+    int32_t channels;
+} ep_cmd_log;
+
+/* Per-channel ring counters, copied to the host by ep_ring_stats_get.
+ * head/tail are cumulative since create/reset; the rest as named. */
+typedef struct {
+    uint64_t head;           /* commands reserved (producers) */
+    uint64_t tail;           /* commands retired (consumer) */
+    uint64_t batches;        /* head reservations (batch pushes) */
+    uint64_t stall_polls;    /* producer polls that found the ring too full */
+    uint32_t max_batch;      /* largest batch pushed */
+    uint32_t max_inflight;   /* largest head - tail a producer observed after reserving */
+    int64_t last_count;      /* commands retired by the last dispatch */
+} ep_ring_stats;
+
+/* Derived launch parameters of a handle (for reports and tests). */
+typedef struct {
+    int32_t rows_per_msg;         /* G in use */
+    int32_t sm_count;             /* SMs of the device */
+    int32_t dispatch_grid;        /* CTAs of the persistent dispatch kernel */
+    int32_t dispatch_stages;      /* shared-memory row stages per dispatch CTA */
+    int32_t dispatch_stage_bytes; /* bytes per stage */
+    int32_t combine_grid;         /* CTAs of the combine kernel */
+    int32_t layout_tiles;         /* token tiles of the layout scan */
+    int32_t reserved;
+    int64_t log_capacity_per_channel;
+    int64_t scratch_bytes;        /* device memory the handle allocated */
+} ep_info;
+
+/* Fill *cfg with the shape and the [UCCL-EP] s5.2 defaults.  Host only. */
+ep_status ep_config_init(ep_config *cfg, int32_t num_ranks, int32_t tokens_per_rank,
+                         int32_t hidden, int32_t num_experts, int32_t topk);
+
+/* Check *cfg without touching the GPU.  Host only. */
+ep_status ep_config_check(const ep_config *cfg);
+
+/* Create a handle on the current device: allocates the rings, their logs and
+ * the layout scratch (cudaMalloc), sized from *cfg.  Synchronous. */
+ep_status ep_create(const ep_config *cfg, ep_handle *out);
+
+/* Free everything ep_create allocated.  Synchronises the device first. */
+ep_status ep_destroy(ep_handle h);
+
+/* Static string for a status code. */
+const char *ep_status_str(ep_status s);
+
+/* Synchronise the device and read the sticky device error word into *code
+ * (EP_OK if none).  Returns EP_OK unless the read itself failed. */
+ep_status ep_last_device_status(ep_handle h, int32_t *code);
+
+/* Synchronise the device, then clear the error word, the rings (head, tail,
+ * slots, statistics) and the layout scan state. */
+ep_status ep_reset(ep_handle h);
+
+/* ep_layout -- token layout of one EP layer ([UCCL-EP] s1: EP needs
+ * fine-grained token-level communication; [NOTES] names a layout/rank mismatch
+ * as an EP failure class).  One single-pass kernel: a warp-aggregated
+ * histogram of picks per (source rank, expert), rank membership per token,
+ * and a decoupled-lookback scan down each destination column giving
+ * token_slot; the last tile to finish derives the small scans.
+ *  topk_idx: device int32 [T, K]; -1 = no pick; other values outside [0, E)
+ *            set EP_ERR_INVALID_ARG on the device and are skipped.
+ *  out:      caller-owned device outputs (all ten pointers required).
+ *  n_recv_host: if non-NULL, the call synchronises `stream` and writes
+ *            N = sum(recv_count), so the caller can size the receive buffer;
+ *            if NULL the call is fully asynchronous. */
+ep_status ep_layout(ep_handle h, const int32_t *topk_idx, const ep_layout_out *out,
+                    int64_t *n_recv_host, void *stream);
+
+/* ep_dispatch -- send every token row to each destination rank it reaches,
+ * once per rank ([UCCL-EP] s6 "Dispatch"; s4.1 pipelined DispatchKernel), and
+ * post one TransferCmd per message of up to G rows into ring d % C in batches
+ * of up to `batch` commands, with producers waiting while a ring holds
+ * max_inflight commands ([UCCL-EP] s2.2 lock-free ring, batch enqueue, flow
+ * control; s4.2 channels).  Consumer warps on the device retire each ring into
+ * its log (ep_cmd_log) and advance its tail; the kernel ends when every ring
+ * is drained ([UCCL-EP] s3.1 Drain).  One persistent cooperative kernel; rows
+ * move by TMA bulk copies through shared memory, each source row read once.
+ *  x:      device bf16 [T, H].
+ *  layout: outputs of ep_layout for this routing (read on the device).
+ *  recv:   device bf16 [recv_capacity_rows, H]; rows [0, N) are written.
+ *          If N > recv_capacity_rows the device sets EP_ERR_CAPACITY and
+ *          nothing is written. */
+ep_status ep_dispatch(ep_handle h, const void *x, const ep_layout_out *layout, void *recv,
+                      int64_t recv_capacity_rows, void *stream);
+
+/* ep_combine -- top-k weighted reduction back to token order ([UCCL-EP] s6
+ * "Combine"):
+ *   out[t] = bf16_rne( acc ), acc = +0.0f; for k = 0..K-1 with a pick:
+ *            acc = fmaf(topk_weights[t][k], expert_out[recv_base[d] + token_slot[t][d]], acc),
+ *            d = topk_idx[t][k] / (E/R)
+ * in fp32, in that fixed order.
+ *  expert_out: device bf16 [expert_out_rows, H] (one row per receive row).
+ *  topk_weights: device fp32 [T, K]; topk_idx: device int32 [T, K].
+ *  out: device bf16 [T, H].  A row index outside [0, expert_out_rows) sets
+ *  EP_ERR_INVALID_ARG on the device and that pick is skipped. */
+ep_status ep_combine(ep_handle h, const void *expert_out, int64_t expert_out_rows,
+                     const float *topk_weights, const int32_t *topk_idx,
+                     const ep_layout_out *layout, void *out, void *stream);
+
+/* Device pointers of the TransferCmd logs (no synchronisation). */
+ep_status ep_cmd_log_get(ep_handle h, ep_cmd_log *out);
+
+/* Copy the ring counters of channels [0, n) to host array out[n]
+ * (synchronises the device).  n must not exceed the channel count. */
+ep_status ep_ring_stats_get(ep_handle h, ep_ring_stats *out, int32_t n);
+
+/* Completion query ([UCCL-EP] s2.2 CheckCompletion): EP_OK if command index
+ * cmd_idx (cumulative since create/reset) of `channel` has been retired by its
+ * consumer, EP_ERR_NOT_READY if not yet.  Synchronous device read. */
+ep_status ep_check_completion(ep_handle h, int32_t channel, uint64_t cmd_idx);
+
+/* Launch parameters and allocation size of a handle.  Host only. */
+ep_status ep_get_info(ep_handle h, ep_info *out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_H_ */

@@ -128,18 +128,23 @@ def layout(num_ranks: int, tokens_per_rank: int, num_experts: int, topk_idx: np.
 
 
 def dispatch(lay: dict, x_bits: np.ndarray, t_begin: int = 0, t_end: int | None = None,
-             recv: np.ndarray | None = None) -> np.ndarray:
+             recv: np.ndarray | None = None, x_first_token: int = 0) -> np.ndarray:
     """recv rows recv_base[d] + token_slot[t][d] <- x[t] (UCCL-EP s6 "Dispatch").
-    x_bits: uint16 [T, H] (bf16 bits).  Returns recv uint16 [n_recv, H]."""
+    x_bits: uint16 [rows, H] (bf16 bits) holding tokens x_first_token onward.
+    Returns recv uint16 [n_recv, H]."""
     lib = _load()
     x_bits = np.ascontiguousarray(x_bits)
-    T, H = x_bits.shape
+    rows, H = x_bits.shape
     R = lay["recv_base"].shape[0]
     if recv is None:
         recv = np.zeros((lay["n_recv"], H), dtype=x_bits.dtype)
-    t_end = T if t_end is None else t_end
-    lib.oracle_dispatch(R, t_begin, t_end, H * x_bits.itemsize, _ptr(lay["token_slot"]),
-                        _ptr(lay["recv_base"]), _ptr(x_bits), _ptr(recv))
+    t_end = x_first_token + rows if t_end is None else t_end
+    assert x_first_token <= t_begin <= t_end <= x_first_token + rows
+    row_bytes = H * x_bits.itemsize
+    # the C routine addresses x by absolute token index
+    x_base = ctypes.c_void_p(x_bits.ctypes.data - x_first_token * row_bytes)
+    lib.oracle_dispatch(R, t_begin, t_end, row_bytes, _ptr(lay["token_slot"]),
+                        _ptr(lay["recv_base"]), x_base, _ptr(recv))
     return recv
 
 

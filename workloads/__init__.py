@@ -129,20 +129,25 @@ def make_x(w: Workload, seed: int | None = None, rows: int | None = None) -> np.
     return bf16_bits_from_f32(rng.standard_normal((T, w.hidden), dtype=np.float32))
 
 
+def _randn_bf16_torch(rows: int, hidden: int, device, seed: int, chunk_rows: int = 65536):
+    """N(0, 1) draws rounded to bf16, generated chunk by chunk on `device`
+    from one seeded generator (deterministic for a given device type)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    out = torch.empty((rows, hidden), dtype=torch.bfloat16, device=device)
+    for r0 in range(0, rows, chunk_rows):
+        r1 = min(rows, r0 + chunk_rows)
+        out[r0:r1] = torch.randn((r1 - r0, hidden), generator=g, device=device, dtype=torch.float32)
+    return out
+
+
 def make_x_torch(w: Workload, device, seed: int | None = None):
     """x ~ N(0, 1) as a bf16 tensor generated directly on `device` (for the
     full-size workloads, where a host-side draw would take long)."""
-    import torch
-    g = torch.Generator(device=device)
-    g.manual_seed((w.seed if seed is None else seed) + 7919)
-    return torch.randn((w.num_tokens, w.hidden), generator=g, device=device,
-                       dtype=torch.float32).to(torch.bfloat16)
+    return _randn_bf16_torch(w.num_tokens, w.hidden, device, (w.seed if seed is None else seed) + 7919)
 
 
 def make_expert_out_torch(rows: int, hidden: int, device, seed: int):
     """A random bf16 expert output [rows, hidden] ~ N(0, 1) on `device`."""
-    import torch
-    g = torch.Generator(device=device)
-    g.manual_seed(seed + 104729)
-    return torch.randn((max(rows, 1), hidden), generator=g, device=device,
-                       dtype=torch.float32).to(torch.bfloat16)[:rows]
+    return _randn_bf16_torch(rows, hidden, device, seed + 104729)
