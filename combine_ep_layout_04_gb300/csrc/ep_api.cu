@@ -70,10 +70,11 @@ ep_status ep_config_check(const ep_config *c) {
         return EP_ERR_INVALID_ARG;
     if (c->topk < 1 || c->topk > ep::kMaxTopk || c->topk > c->num_experts) return EP_ERR_INVALID_ARG;
     if (c->channels < 1 || c->channels > ep::kMaxChannels) return EP_ERR_INVALID_ARG;
-    if (!is_pow2(c->ring_depth) || c->ring_depth < 8 || c->ring_depth > 65536) return EP_ERR_INVALID_ARG;
+    // rings live in shared memory: 16 bytes a slot
+    if (!is_pow2(c->ring_depth) || c->ring_depth < 8 || c->ring_depth > 8192) return EP_ERR_INVALID_ARG;
     if (c->max_inflight < 8 || c->max_inflight > c->ring_depth) return EP_ERR_INVALID_ARG;
     if (c->batch < 1 || c->batch > 8) return EP_ERR_INVALID_ARG;
-    if (c->rows_per_msg < 0 || c->rows_per_msg > (1 << 20)) return EP_ERR_INVALID_ARG;
+    if (c->rows_per_msg < 0 || c->rows_per_msg > 2047) return EP_ERR_INVALID_ARG;   // 11 bits in a ring slot
     if (c->drain_batch < 32 || c->drain_batch > 512 || c->drain_batch % 32 != 0) return EP_ERR_INVALID_ARG;
     if (c->debug_flags & ~EP_DEBUG_DISABLE_CONSUMER) return EP_ERR_INVALID_ARG;
     const int64_t T = static_cast<int64_t>(c->num_ranks) * c->tokens_per_rank;
@@ -108,7 +109,7 @@ ep_status ep_create(const ep_config *cfg, ep_handle *out) {
     h->cfg = *cfg;
     if (h->cfg.timeout_ns == 0) h->cfg.timeout_ns = ep::kDefaultTimeoutNs;
     h->G = cfg->rows_per_msg ? cfg->rows_per_msg : default_rows_per_msg(cfg->hidden);
-    const int R = cfg->num_ranks, E = cfg->num_experts, C = cfg->channels, D = cfg->ring_depth;
+    const int R = cfg->num_ranks, E = cfg->num_experts, C = cfg->channels;
     const int64_t Tpr = cfg->tokens_per_rank, T = R * Tpr;
     if (cudaGetDevice(&h->device) != cudaSuccess ||
         cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
@@ -116,7 +117,6 @@ ep_status ep_create(const ep_config *cfg, ep_handle *out) {
         return EP_ERR_CUDA;
     }
     h->tiles = static_cast<int>((T + 255) / 256);
-    h->msgs_per_pair = static_cast<int>((Tpr + h->G - 1) / h->G);
     // log capacity: every message of every (s, d) with d in the busiest channel
     const int64_t ranks_per_chan = (R + C - 1) / C;
     const int64_t kmin = cfg->topk < ranks_per_chan ? cfg->topk : ranks_per_chan;
@@ -134,15 +134,15 @@ ep_status ep_create(const ep_config *cfg, ep_handle *out) {
     const size_t o_hist = cv.take<int32_t>(static_cast<size_t>(R) * E);
     const size_t o_pref = cv.take<int32_t>(static_cast<size_t>(R + 1) * R);
     const size_t o_nrecv = cv.take<int64_t>(1);
-    const size_t o_slots = cv.take<ep_transfer_cmd>(static_cast<size_t>(C) * D);
-    const size_t o_status = cv.take<unsigned long long>(static_cast<size_t>(C) * D);
     const size_t o_head = cv.take<unsigned long long>(static_cast<size_t>(C) * ep::kHeadStride);
     const size_t o_tail = cv.take<unsigned long long>(static_cast<size_t>(C) * ep::kHeadStride);
     const size_t o_stats = cv.take<ep::RingStatsDev>(C);
     const size_t o_log = cv.take<ep_transfer_cmd>(static_cast<size_t>(C) * h->log_cap);
     const size_t o_lcount = cv.take<int64_t>(C);
-    const size_t n_fill = h->G > 1 ? static_cast<size_t>(R) * R * h->msgs_per_pair : 0;
-    const size_t o_fill = cv.take<unsigned int>(n_fill > 0 ? n_fill : 1);
+    const size_t o_notice = cv.take<int32_t>(static_cast<size_t>(h->nchunks) * 2 * R);
+    const size_t o_ready = cv.take<unsigned int>(static_cast<size_t>(h->nchunks));
+    const size_t o_gen = cv.take<unsigned int>(1);
+    const size_t o_ddone = cv.take<unsigned int>(1);
     h->alloc_bytes = cv.off;
     if (cudaMalloc(&h->alloc_base, h->alloc_bytes) != cudaSuccess) {
         delete h;
@@ -162,14 +162,15 @@ ep_status ep_create(const ep_config *cfg, ep_handle *out) {
     d.hist = reinterpret_cast<int32_t *>(b + o_hist);
     d.col_prefix = reinterpret_cast<int32_t *>(b + o_pref);
     d.n_recv = reinterpret_cast<int64_t *>(b + o_nrecv);
-    d.slots = reinterpret_cast<ep_transfer_cmd *>(b + o_slots);
-    d.status = reinterpret_cast<unsigned long long *>(b + o_status);
     d.head = reinterpret_cast<unsigned long long *>(b + o_head);
     d.tail = reinterpret_cast<unsigned long long *>(b + o_tail);
     d.stats = reinterpret_cast<ep::RingStatsDev *>(b + o_stats);
     d.log = reinterpret_cast<ep_transfer_cmd *>(b + o_log);
     d.log_count = reinterpret_cast<int64_t *>(b + o_lcount);
-    d.msg_fill = n_fill > 0 ? reinterpret_cast<unsigned int *>(b + o_fill) : nullptr;
+    d.notice = reinterpret_cast<int32_t *>(b + o_notice);
+    d.ready = reinterpret_cast<unsigned int *>(b + o_ready);
+    d.disp_gen = reinterpret_cast<unsigned int *>(b + o_gen);
+    d.disp_done = reinterpret_cast<unsigned int *>(b + o_ddone);
     if (cudaDeviceSynchronize() != cudaSuccess) {
         cudaFree(h->alloc_base);
         delete h;
@@ -279,16 +280,12 @@ ep_status ep_ring_stats_get(ep_handle h, ep_ring_stats *out, int32_t n) {
 ep_status ep_check_completion(ep_handle h, int32_t channel, uint64_t cmd_idx) {
     if (!h || channel < 0 || channel >= h->cfg.channels) return EP_ERR_INVALID_ARG;
     if (cudaDeviceSynchronize() != cudaSuccess) return EP_ERR_CUDA;
-    unsigned long long tail = 0, status = 0;
-    const size_t sidx = static_cast<size_t>(channel) * h->cfg.ring_depth + (cmd_idx & (h->cfg.ring_depth - 1));
+    unsigned long long tail = 0;
     if (cudaMemcpy(&tail, h->dev.tail + static_cast<size_t>(channel) * ep::kHeadStride, sizeof(tail),
-                   cudaMemcpyDeviceToHost) != cudaSuccess ||
-        cudaMemcpy(&status, h->dev.status + sidx, sizeof(status), cudaMemcpyDeviceToHost) != cudaSuccess)
+                   cudaMemcpyDeviceToHost) != cudaSuccess)
         return EP_ERR_CUDA;
-    // retired: the slot still holds this command marked COMPLETED, or the tail
-    // has moved past it
-    if (status == 2ull * cmd_idx + 2ull || tail > cmd_idx) return EP_OK;
-    return EP_ERR_NOT_READY;
+    // a command is complete once the consumer's tail has moved past it
+    return tail > cmd_idx ? EP_OK : EP_ERR_NOT_READY;
 }
 
 ep_status ep_get_info(ep_handle h, ep_info *out) {

@@ -5,8 +5,9 @@
 // commands and flow control against kMaxInflight; s2.3 the TransferCmd fields
 // {dst_rank, src_offset, dst_offset, size}; s3.1 Write completes when the
 // target memory is visible, Drain waits until the queue is empty; s4.1 the
-// pipelined DispatchKernel and packing of small tokens; s4.2 independent
-// channels; NCCL GIN article s2.2.1 byte-offset windows):
+// pipelined DispatchKernel -- prepare, then post, then go on -- and packing of
+// small tokens; s4.2 independent channels; NCCL GIN article s2.2.1 byte-offset
+// windows):
 //
 //   for every token t and destination rank d with token_slot[t][d] >= 0:
 //       recv[recv_base[d] + token_slot[t][d]] <- x[t]        (one copy per rank)
@@ -14,72 +15,98 @@
 //       post TransferCmd{d, rows*B, (send_off[s][d] + gG)*B, (recv_off[s][d] + gG)*B}
 //       into ring d % C once all its rows have landed.
 //
-// How: one persistent cooperative kernel, one CTA per SM, three warps:
-//   warp 0  copy warp: 1-D TMA bulk loads of token rows (a run of whole rows
-//           when they are small, a piece of one row when it is large) into a
-//           ring of shared-memory stages, then one TMA bulk store per
-//           (row, destination) from the stage; each source row is read from
-//           HBM once whatever its number of destinations.  Lane 0 issues the
+// How: one persistent cooperative kernel, one CTA per SM, in two kinds.
+//
+// Copy CTAs (all but the first C) move the rows.  Chunks of 32 tokens of one
+// source rank are dealt to them round-robin; three warps hand each chunk on
+// through mbarriers and shared counters:
+//   copy    1-D TMA bulk loads of token rows (a run of whole rows when they
+//           are small, a piece of one row when it is large) into a ring of
+//           shared-memory stages, then one TMA bulk store per (row,
+//           destination) from the stage; each source row is read from HBM
+//           once whatever its number of destinations.  Lane 0 issues the
 //           loads; all 32 lanes issue stores, each tracking its own bulk
-//           groups, so that a stage is recycled only when every lane's stores
-//           from it have completed.
-//   warp 1  meta/post warp: per chunk of 32 tokens of one source rank, reads
-//           the token_slot rows, builds each token's destination-row list and
-//           each rank's slot range for the copy warp, and -- once the copy
-//           warp reports the chunk's stores complete -- works out which
-//           messages the chunk completed (a message whose rows were written by
-//           several CTAs is completed by whichever CTA lands its last row,
-//           counted with one atomic per CTA and message) and posts them,
-//           grouped per ring into batches of up to `batch` commands: reserve
-//           with one atomicAdd on head, wait (bounded) while the ring would
-//           exceed max_inflight, write the records, publish each slot with a
-//           release store of its sequence tag.
-//   warp 2  (CTAs 0..C-1) ring consumer for channel blockIdx.x: each step
-//           polls every slot that can be outstanding (max_inflight of them,
-//           drain_batch = 32 per warp-wide poll, all loads in flight at once),
-//           retires the longest published run into the channel's log, marks
-//           those slots COMPLETED and advances tail with one release store; it
-//           stops when the channel's message count (from msg_count) has been
-//           retired, which is the drain.
+//           groups, so a stage is recycled only once every lane's stores from
+//           it have completed.
+//   meta    reads the chunk's token_slot rows; builds each token's
+//           destination-row list (for the copy warp) and writes the chunk's
+//           notice -- the first and last window slot it covers per
+//           destination rank -- to global memory.
+//   notify  once the chunk's stores are complete, fences and sets the
+//           chunk's ready flag (tagged with the dispatch's generation).
+//
+// Channel CTAs (the first C) each own ring c = blockIdx.x:
+//   poster  walks every chunk in order, waits for its ready flag, and turns
+//           its notice into the messages of ring c that the chunk completes:
+//           a message of G rows is complete in the chunk that holds its last
+//           row, since all earlier rows of the pair are in earlier chunks.
+//           It posts them in batches of up to `batch` commands: one atomicAdd
+//           on head per batch, a wait while the ring would hold more than
+//           max_inflight commands, then the slot stores.
+//   poller  examines every slot that can be outstanding (drain_batch = 32 per
+//           warp-wide load), takes the longest run of published slots, stages
+//           the records for the logger and moves the tail (the retire point)
+//           -- the posters read it in shared memory, so flow control costs no
+//           round trip.
+//   logger  decodes the staged records into TransferCmds, appends them to the
+//           channel's log in device memory and publishes the cumulative tail
+//           and head there (a command is complete once tail has passed it).
+//   The channel finishes when its message count (from msg_count) has been
+//   retired: the drain.
+//
+// A ring lives in its channel CTA's shared memory -- the CTA's posters and
+// consumer are its only users -- as self-validating 16-byte records (see
+// lap_tag): posting a command is one store, reading it needs no fence, and a
+// turn of the ring costs no L2 round trip (which takes microseconds while the
+// copy CTAs saturate HBM).  The cumulative head and tail the host reads, and
+// the logs, are in device memory.  The copy path never waits on a ring.
 // Every wait is bounded by the handle's timeout and by the grid's error word;
-// none traps.  A cooperative launch keeps all CTAs -- and so all consumers --
-// resident while producers wait on them.
+// none traps.  A cooperative launch keeps every CTA resident while others
+// wait on it.
 #include "ep_internal.cuh"
 
 namespace ep {
 namespace {
 
-constexpr int kThreads = 96;
+constexpr int kThreads = 192;   // copy CTAs use warps 0-2; channel CTAs 0-5
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kCopyWarp = 0, kMetaWarp = 1, kConsumerWarp = 2;
+constexpr int kMetaSlots = 3;       // destination lists in flight (copy CTAs)
+constexpr int kDoneSlots = 16;      // chunks stored but not yet reported complete
+constexpr int kPrefetchItems = 4;   // row loads in flight per copy CTA
+constexpr int kStoreLagItems = 2;   // items whose stores may still be in flight
+constexpr int kMaxPollRounds = 16;  // up to 512 slots examined per consumer step
+constexpr int kLogStage = 1024;     // staged records (16 bytes each) awaiting the logger
 
 // Shared-memory carve, identical on host and device.
 struct SmemLayout {
     int stage_off, meta_off, meta_slot_bytes, scratch_off, bar_off, total;
-    // meta slot (ints): dst[32*R] | pref[33] | lo[R] | hi[R] | info[4]
-    __host__ __device__ static int meta_ints(int R) { return ((32 * R + 33 + 2 * R + 4) + 3) & ~3; }
-    __host__ __device__ SmemLayout(int R, int C, int stage_bytes, int stages, int meta_slots) {
+    __host__ __device__ static int ring_off(int R) { return ((12 * R * R) + 127) / 128 * 128; }
+    __host__ __device__ SmemLayout(int R, int D, int stage_bytes, int stages) {
         stage_off = 0;
-        meta_off = stage_bytes * stages;
-        meta_slot_bytes = meta_ints(R) * 4;
-        scratch_off = meta_off + meta_slot_bytes * meta_slots;
-        // scratch ints: rbase[R] | nd[R] | gs[R] | ctot[C] | cbb[C+1] | flags[4]
-        const int scratch_ints = (3 * R + 2 * C + 1 + 4 + 3) & ~3;
-        bar_off = (scratch_off + scratch_ints * 4 + 15) & ~15;
-        total = bar_off + 8 * (stages + 2 * meta_slots);
+        // channel CTAs keep the pair tables (3 x R x R ints) and their ring
+        // (D slots of 16 bytes) where copy CTAs keep their stages
+        const int stage_area = stage_bytes * stages, channel = ring_off(R) + 16 * D + 16 * kLogStage;
+        meta_off = stage_area > channel ? stage_area : channel;
+        meta_slot_bytes = ((32 * R + 33) + 3) / 4 * 16;   // dst[32*R] | pref[33]
+        scratch_off = meta_off + meta_slot_bytes * kMetaSlots;
+        // scratch: rbase[R] ints, then 8 u64 words (flags, progress counters)
+        bar_off = (scratch_off + ((R + 3) & ~3) * 4 + 64 + 15) & ~15;
+        total = bar_off + 8 * (stages + 2 * kMetaSlots);
     }
 };
 
 struct MetaSlot {
-    int *dst, *pref, *lo, *hi, *info;   // info: chunk, ntok, src rank, first token
+    int *dst, *pref;
     __device__ MetaSlot(uint8_t *base, int R) {
         dst = reinterpret_cast<int *>(base);
         pref = dst + 32 * R;
-        lo = pref + 33;
-        hi = lo + R;
-        info = hi + R;
     }
 };
+
+// Shared words (u64) after rbase: abort flag; chunks complete (copy CTA) or
+// ring tail = retire point (channel CTA); poller stopped; ring base; dispatch
+// generation; messages expected on the channel; ring head; records logged.
+enum { kWAbort = 0, kWProgress = 1, kWStopped = 2, kWBase = 3, kWGen = 4, kWExpected = 5, kWHead = 6, kWLogged = 7 };
 
 __device__ __forceinline__ int chunk_ntok(const DispatchParams &p, int k) {
     const int ci = k % p.chunks_per_rank;
@@ -92,14 +119,23 @@ __device__ __forceinline__ int64_t chunk_tok0(const DispatchParams &p, int k) {
 __device__ __forceinline__ int chunk_items(const DispatchParams &p, int ntok) {
     return p.pieces > 1 ? ntok * p.pieces : (ntok + p.rows_per_item - 1) / p.rows_per_item;
 }
+// Copy CTA q of NQ takes chunks q, q + NQ, ...
+__device__ __forceinline__ int my_chunks(const DispatchParams &p, int q, int NQ) {
+    return q < p.nchunks ? (p.nchunks - q + NQ - 1) / NQ : 0;
+}
 
-// Walks this CTA's items: chunks blockIdx.x, +gridDim.x, ...; items within.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const DispatchParams &p) {
+    return __all_sync(kFull, mbar_wait_bounded(bar, parity, p.dev.err, p.timeout_ns));
+}
+
+// Walks a copy CTA's items: chunks q, q + NQ, ...; items within each.
 struct ItemCursor {
-    int m, k, q, ntok, nitems;
+    int m, k, q, ntok, nitems, step;
     bool valid;
-    __device__ void start(const DispatchParams &p) {
+    __device__ void start(const DispatchParams &p, int first, int NQ) {
         m = 0;
-        k = blockIdx.x;
+        k = first;
+        step = NQ;
         q = 0;
         valid = k < p.nchunks;
         if (valid) {
@@ -111,7 +147,7 @@ struct ItemCursor {
         if (++q < nitems) return;
         q = 0;
         ++m;
-        k += gridDim.x;
+        k += step;
         valid = k < p.nchunks;
         if (valid) {
             ntok = chunk_ntok(p, k);
@@ -134,18 +170,24 @@ struct ItemCursor {
     }
 };
 
-// ------------------------------------------------------------------ copy warp
-__device__ void copy_warp(const DispatchParams &p, uint8_t *smem, const SmemLayout &L, uint64_t *bar_full,
-                          uint64_t *meta_full, uint64_t *chunk_done) {
+struct Bars {
+    uint64_t *stage_full, *meta_full, *meta_free;
+};
+
+// ------------------------------------------------------------ copy CTA: copy
+__device__ void copy_warp(const DispatchParams &p, uint8_t *smem, const SmemLayout &L, const Bars &bars, int qcta,
+                          int NQ, unsigned long long *words) {
     const int lane = threadIdx.x & 31;
-    const int S = p.stages, P = p.prefetch, NS = p.meta_slots;
+    const int S = p.stages, P = p.prefetch;
     const int64_t B = p.row_bytes;
     ItemCursor ld, stc;
-    ld.start(p);
-    stc.start(p);
+    ld.start(p, qcta, NQ);
+    stc.start(p, qcta, NQ);
     int64_t n_loaded = 0, n_stored = 0;
-    int stored_chunks = 0, signalled = 0;
-    int64_t last_item[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // last item of in-flight chunks (NS <= 8)
+    int stored_chunks = 0, reported = 0;
+    int64_t last_item[kDoneSlots];   // last item of chunks stored but not yet reported
+#pragma unroll
+    for (int i = 0; i < kDoneSlots; ++i) last_item[i] = 0;
     bool ok = true;
 
     auto issue_load = [&](const ItemCursor &c, int64_t idx) {
@@ -155,17 +197,20 @@ __device__ void copy_warp(const DispatchParams &p, uint8_t *smem, const SmemLayo
             const int stage = static_cast<int>(idx % S);
             const uint32_t bytes = static_cast<uint32_t>((tb - ta) * len);
             const uint8_t *src = p.x + (chunk_tok0(p, c.k) + ta) * B + off;
-            mbar_arrive_expect_tx(&bar_full[stage], bytes);
-            bulk_g2s(smem + L.stage_off + static_cast<int64_t>(stage) * p.stage_bytes, src, bytes, &bar_full[stage]);
+            mbar_arrive_expect_tx(&bars.stage_full[stage], bytes);
+            bulk_g2s(smem + L.stage_off + static_cast<int64_t>(stage) * p.stage_bytes, src, bytes,
+                     &bars.stage_full[stage]);
         }
     };
-    // Signal every stored chunk whose last item is <= upto as complete.
-    auto signal_upto = [&](int64_t upto) {
-        fence_proxy_async_global();
-        __syncwarp();
-        while (signalled < stored_chunks && last_item[signalled % NS] <= upto) {
-            if (lane == 0) mbar_arrive(&chunk_done[signalled % NS]);
-            ++signalled;
+    // Report every stored chunk whose last item is <= upto as complete (the
+    // notify warp reads the count).
+    auto report_upto = [&](int64_t upto) {
+        const int before = reported;
+        while (reported < stored_chunks && last_item[reported % kDoneSlots] <= upto) ++reported;
+        if (reported != before) {
+            fence_proxy_async_global();
+            __syncwarp();
+            if (lane == 0) st_release_cta_shared(&words[kWProgress], static_cast<unsigned long long>(reported));
         }
     };
 
@@ -175,15 +220,14 @@ __device__ void copy_warp(const DispatchParams &p, uint8_t *smem, const SmemLayo
     }
     while (stc.valid) {
         const int64_t i = n_stored;
-        const int slot = stc.m % NS;
+        const int slot = stc.m % kMetaSlots;
         if (stc.q == 0) {
-            const uint32_t par = static_cast<uint32_t>(stc.m / NS) & 1u;
-            // warp-uniform decisions: a phase may complete between two lanes' tests
-            if (!__all_sync(kFull, mbar_test(&meta_full[slot], par))) {
-                // the meta warp may be waiting for earlier chunks: complete them first
+            const uint32_t par = static_cast<uint32_t>(stc.m / kMetaSlots) & 1u;
+            if (!__all_sync(kFull, mbar_test(&bars.meta_full[slot], par))) {
+                // report what has landed before waiting on the meta warp
                 bulk_wait<0>();
-                signal_upto(INT64_MAX);
-                if (!__all_sync(kFull, mbar_wait_bounded(&meta_full[slot], par, p.dev.err, p.timeout_ns))) {
+                report_upto(INT64_MAX);
+                if (!warp_wait(&bars.meta_full[slot], par, p)) {
                     set_error(p.dev.err, EP_ERR_TIMEOUT);
                     ok = false;
                     break;
@@ -191,8 +235,7 @@ __device__ void copy_warp(const DispatchParams &p, uint8_t *smem, const SmemLayo
             }
         }
         const int stage = static_cast<int>(i % S);
-        if (!__all_sync(kFull, mbar_wait_bounded(&bar_full[stage], static_cast<uint32_t>(i / S) & 1u, p.dev.err,
-                                                 p.timeout_ns))) {
+        if (!warp_wait(&bars.stage_full[stage], static_cast<uint32_t>(i / S) & 1u, p)) {
             set_error(p.dev.err, EP_ERR_TIMEOUT);
             ok = false;
             break;
@@ -213,32 +256,37 @@ __device__ void copy_warp(const DispatchParams &p, uint8_t *smem, const SmemLayo
             bulk_commit();
         }
         if (stc.q == stc.nitems - 1) {
-            last_item[stc.m % NS] = i;
+            // every store of the chunk is issued: its destination list is free
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.meta_free[slot]);
+            last_item[stc.m % kDoneSlots] = i;
             ++stored_chunks;
         }
         ++n_stored;
         stc.advance(p);
+        // At most store_lag items' stores stay in flight; the stage of item
+        // n_loaded was last used by item n_loaded - S, complete because
+        // store_lag <= S - P.
+        bulk_wait_n(p.store_lag);
+        report_upto(n_stored - 1 - p.store_lag);
         if (ld.valid) {
-            // stage of item n_loaded was last used by item n_loaded - S
-            bulk_wait_n(S - P);
-            signal_upto(n_stored - 1 - (S - P));
             issue_load(ld, n_loaded++);
             ld.advance(p);
         }
     }
     bulk_wait<0>();
     if (ok) {
-        signal_upto(INT64_MAX);
+        report_upto(INT64_MAX);
     } else {
         // abort: let every load already issued land before the CTA exits (the
         // wait ignores the error word; it is still bounded by the time limit)
         for (int64_t j = n_stored; j < n_loaded; ++j)
-            mbar_wait_bounded(&bar_full[j % S], static_cast<uint32_t>(j / S) & 1u, nullptr, p.timeout_ns);
+            mbar_wait_bounded(&bars.stage_full[j % S], static_cast<uint32_t>(j / S) & 1u, nullptr, p.timeout_ns);
         __syncwarp();
     }
 }
 
-// ------------------------------------------------------------ meta/post warp
+// ------------------------------------------------------------ copy CTA: meta
 __device__ void build_meta(const DispatchParams &p, int k, const MetaSlot &ms, const int *rbase) {
     const int lane = threadIdx.x & 31;
     const int R = p.R;
@@ -246,6 +294,7 @@ __device__ void build_meta(const DispatchParams &p, int k, const MetaSlot &ms, c
     const int64_t tok0 = chunk_tok0(p, k);
     const bool valid = lane < ntok;
     const int64_t t = tok0 + lane;
+    int32_t *notice = p.dev.notice + static_cast<int64_t>(k) * 2 * R;
     int n = 0;
     int *dst = ms.dst + lane * R;
     for (int d0 = 0; d0 < R; d0 += 4) {
@@ -273,9 +322,9 @@ __device__ void build_meta(const DispatchParams &p, int k, const MetaSlot &ms, c
             }
             const int lo = __reduce_min_sync(kFull, sl >= 0 ? sl : INT32_MAX);
             const int hi = __reduce_max_sync(kFull, sl >= 0 ? sl : -1);
-            if (lane == 0) {
-                ms.lo[d] = lo == INT32_MAX ? -1 : lo;
-                ms.hi[d] = hi;
+            if (lane == (d & 31)) {
+                notice[2 * d] = lo == INT32_MAX ? -1 : lo;
+                notice[2 * d + 1] = hi;
             }
         }
     }
@@ -287,250 +336,302 @@ __device__ void build_meta(const DispatchParams &p, int k, const MetaSlot &ms, c
     }
     ms.pref[lane] = incl - n;
     if (lane == 31) ms.pref[32] = incl;
-    if (lane == 0) {
-        ms.info[0] = k;
-        ms.info[1] = ntok;
-        ms.info[2] = k / p.chunks_per_rank;
-        ms.info[3] = 0;
-    }
 }
 
-// Rows of message g of a pair with cnt rows.
-__device__ __forceinline__ int msg_rows(int g, int G, int cnt) { return min(G, cnt - g * G); }
-
-// Adds `rows` landed rows to message (s, d, g); true if this call completed it.
-__device__ __forceinline__ bool message_fill(const DispatchParams &p, int s, int d, int g, int rows, int need) {
-    if (g < 0 || g >= p.msgs_per_pair) {
-        set_error(p.dev.err, EP_ERR_INVALID_ARG);
-        return false;
-    }
-    unsigned int *ctr = p.dev.msg_fill + (static_cast<int64_t>(s) * p.R + d) * p.msgs_per_pair + g;
-    const unsigned old = atomicAdd(ctr, static_cast<unsigned>(rows));
-    if (old + static_cast<unsigned>(rows) == static_cast<unsigned>(need)) {
-        *ctr = 0u;   // last arrival: leave it zeroed for the next call
-        __threadfence();
-        return true;
-    }
-    return false;
-}
-
-// Posts n commands of channel c, flat indices [f0, f0 + n) of this chunk's list.
-__device__ bool post_batch(const DispatchParams &p, int c, int s, int f0, int n, const int *nd, const int *gs) {
-    unsigned long long *head = p.dev.head + static_cast<int64_t>(c) * kHeadStride;
-    unsigned long long *tail = p.dev.tail + static_cast<int64_t>(c) * kHeadStride;
-    const unsigned long long base = atomicAdd(head, static_cast<unsigned long long>(n));
-    unsigned long long tl = ld_acquire(tail);
-    unsigned long long stalls = 0;
-    if (base + n - tl > static_cast<unsigned long long>(p.max_inflight)) {
-        const uint64_t t0 = globaltimer_ns();
-        unsigned sleep = 32;
-        while (true) {
-            __nanosleep(sleep);
-            sleep = min(sleep * 2u, 1024u);
-            tl = ld_acquire(tail);
-            ++stalls;
-            if (base + n - tl <= static_cast<unsigned long long>(p.max_inflight)) break;
-            if (read_error(p.dev.err) != 0) return false;
-            if (globaltimer_ns() - t0 > p.timeout_ns) {
-                set_error(p.dev.err, EP_ERR_TIMEOUT);
-                return false;
-            }
-        }
-    }
-    const int R = p.R, G = p.G, C = p.C;
-    const int64_t B = p.row_bytes;
-    for (int i = 0; i < n; ++i) {
-        int f = f0 + i, d = c;
-        while (d < R && f >= nd[d]) {
-            f -= nd[d];
-            d += C;
-        }
-        if (d >= R) {   // cannot happen with a consistent list
-            set_error(p.dev.err, EP_ERR_INVALID_ARG);
-            return false;
-        }
-        const int g = gs[d] + f;
-        const int j0 = g * G;
-        const int cnt = __ldg(p.cnt + s * R + d);
-        const int rows = msg_rows(g, G, cnt);
-        const unsigned long long idx = base + i;
-        const int64_t sidx = static_cast<int64_t>(c) * p.D + static_cast<int64_t>(idx & static_cast<unsigned long long>(p.D - 1));
-        uint4 *rec = reinterpret_cast<uint4 *>(p.dev.slots + sidx);
-        const uint64_t src_off = static_cast<uint64_t>((static_cast<int64_t>(__ldg(p.send_off + s * R + d)) + j0) * B);
-        const uint64_t dst_off = static_cast<uint64_t>((static_cast<int64_t>(__ldg(p.recv_off + s * R + d)) + j0) * B);
-        rec[0] = make_uint4(static_cast<uint32_t>(d), static_cast<uint32_t>(rows * B), static_cast<uint32_t>(src_off),
-                            static_cast<uint32_t>(src_off >> 32));
-        rec[1] = make_uint4(static_cast<uint32_t>(dst_off), static_cast<uint32_t>(dst_off >> 32), 0u, 0u);
-        st_release(p.dev.status + sidx, 2ull * idx + 1ull);
-    }
-    RingStatsDev *stt = p.dev.stats + c;
-    atomicAdd(&stt->batches, 1ull);
-    atomicMax(&stt->max_batch, static_cast<unsigned>(n));
-    atomicMax(&stt->max_inflight, static_cast<unsigned>(base + n - tl));
-    if (stalls) atomicAdd(&stt->stall_polls, stalls);
-    return true;
-}
-
-// After the chunk's rows have landed: the chunk's completed messages, posted.
-__device__ bool post_chunk(const DispatchParams &p, const MetaSlot &ms, int *nd, int *gs, int *ctot, int *cbb) {
+__device__ void meta_warp(const DispatchParams &p, uint8_t *smem, const SmemLayout &L, const Bars &bars,
+                          const int *rbase, int qcta, int NQ) {
     const int lane = threadIdx.x & 31;
-    const int R = p.R, C = p.C, G = p.G;
-    const int s = ms.info[2];
-    __threadfence();   // this CTA's rows are visible before any count or record
-    for (int d = lane; d < R; d += 32) {
-        const int lo = ms.lo[d], hi = ms.hi[d];
-        int n = 0, g_start = 0;
-        if (hi >= 0) {
-            const int ro = __ldg(p.recv_off + s * R + d);
-            const int cnt = __ldg(p.cnt + s * R + d);
-            const int jlo = lo - ro, jhi = hi - ro;
-            if (jlo < 0 || jhi < jlo || jhi >= cnt) {
-                set_error(p.dev.err, EP_ERR_INVALID_ARG);
-            } else {
-                const int ga = jlo / G, gb = jhi / G;
-                int m0 = ga * G, m1 = m0 + msg_rows(ga, G, cnt) - 1;
-                int in_lo = max(m0, jlo), in_hi = min(m1, jhi);
-                bool done = (in_lo == m0 && in_hi == m1) ||
-                            message_fill(p, s, d, ga, in_hi - in_lo + 1, m1 - m0 + 1);
-                g_start = done ? ga : ga + 1;
-                int g_end = ga + 1;
-                if (gb > ga) {
-                    m0 = gb * G;
-                    m1 = m0 + msg_rows(gb, G, cnt) - 1;
-                    in_hi = min(m1, jhi);
-                    done = (in_hi == m1) || message_fill(p, s, d, gb, in_hi - m0 + 1, m1 - m0 + 1);
-                    g_end = done ? gb + 1 : gb;
-                }
-                n = max(0, g_end - g_start);
-            }
-        }
-        nd[d] = n;
-        gs[d] = g_start;
-    }
-    __syncwarp();
-    for (int c = lane; c < C; c += 32) {
-        int tot = 0;
-        for (int d = c; d < R; d += C) tot += nd[d];
-        ctot[c] = tot;
-    }
-    __syncwarp();
-    if (lane == 0) {
-        int run = 0;
-        for (int c = 0; c < C; ++c) {
-            cbb[c] = run;
-            run += (ctot[c] + p.batch - 1) / p.batch;
-        }
-        cbb[C] = run;
-    }
-    __syncwarp();
-    const int nb = cbb[C];
-    bool ok = true;
-    for (int b = lane; b < nb; b += 32) {
-        int c = 0;
-        while (cbb[c + 1] <= b) ++c;
-        const int f0 = (b - cbb[c]) * p.batch;
-        const int n = min(p.batch, ctot[c] - f0);
-        if (!post_batch(p, c, s, f0, n, nd, gs)) {
-            ok = false;
-            break;
-        }
-    }
-    return __all_sync(kFull, ok);
-}
-
-__device__ void meta_warp(const DispatchParams &p, uint8_t *smem, const SmemLayout &L, uint64_t *meta_full,
-                          uint64_t *chunk_done, int *scratch) {
-    const int lane = threadIdx.x & 31;
-    const int R = p.R, C = p.C, NS = p.meta_slots;
-    int *rbase = scratch, *nd = scratch + R, *gs = scratch + 2 * R, *ctot = scratch + 3 * R, *cbb = ctot + C;
-    auto slot_of = [&](int m) {
-        return MetaSlot(smem + L.meta_off + static_cast<int64_t>(m % NS) * L.meta_slot_bytes, R);
-    };
-    int n_my = 0;
-    for (int m = 0;; ++m) {
-        const int k = blockIdx.x + m * gridDim.x;
-        if (k >= p.nchunks) break;
-        n_my = m + 1;
-        if (m >= NS) {
-            const int mm = m - NS;
-            if (!__all_sync(kFull, mbar_wait_bounded(&chunk_done[mm % NS], static_cast<uint32_t>(mm / NS) & 1u,
-                                                     p.dev.err, p.timeout_ns))) {
-                set_error(p.dev.err, EP_ERR_TIMEOUT);
-                return;
-            }
-            if (!post_chunk(p, slot_of(mm), nd, gs, ctot, cbb)) return;
-        }
-        build_meta(p, k, slot_of(m), rbase);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&meta_full[m % NS]);
-    }
-    for (int mm = max(0, n_my - NS); mm < n_my; ++mm) {
-        if (!__all_sync(kFull, mbar_wait_bounded(&chunk_done[mm % NS], static_cast<uint32_t>(mm / NS) & 1u,
-                                                 p.dev.err, p.timeout_ns))) {
+    const int n_my = my_chunks(p, qcta, NQ);
+    for (int m = 0; m < n_my; ++m) {
+        const int k = qcta + m * NQ;
+        if (m >= kMetaSlots &&
+            !warp_wait(&bars.meta_free[m % kMetaSlots], static_cast<uint32_t>(m / kMetaSlots - 1) & 1u, p)) {
             set_error(p.dev.err, EP_ERR_TIMEOUT);
             return;
         }
-        if (!post_chunk(p, slot_of(mm), nd, gs, ctot, cbb)) return;
+        build_meta(p, k, MetaSlot(smem + L.meta_off + static_cast<int64_t>(m % kMetaSlots) * L.meta_slot_bytes, p.R),
+                   rbase);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.meta_full[m % kMetaSlots]);
     }
 }
 
-// ------------------------------------------------------------ consumer warp
-constexpr int kMaxPollRounds = 16;   // up to 512 slots examined per step
+// ---------------------------------------------------------- copy CTA: notify
+// Sets ready[k] once chunk k's rows are complete: the copy warp counts
+// completed chunks in shared memory; one gpu-scope fence covers every chunk
+// reported since the last one.
+__device__ void notify_warp(const DispatchParams &p, int qcta, int NQ, unsigned long long *words) {
+    if ((threadIdx.x & 31) != 0) return;
+    const int n_my = my_chunks(p, qcta, NQ);
+    const unsigned int tag = static_cast<unsigned int>(words[kWGen]) + 1u;
+    int done = 0;
+    uint64_t idle_since = globaltimer_ns();
+    unsigned sleep = 32;
+    while (done < n_my) {
+        const int now = static_cast<int>(ld_acquire_cta_shared(&words[kWProgress]));
+        if (now > done) {
+            fence_acq_rel_gpu();   // the chunks' rows are visible device-wide before their flags
+            for (int m = done; m < now; ++m)
+                st_relaxed_u32(p.dev.ready + qcta + static_cast<int64_t>(m) * NQ, tag);
+            done = now;
+            idle_since = globaltimer_ns();
+            sleep = 32;
+            continue;
+        }
+        if (read_error(p.dev.err) != 0) break;
+        if (globaltimer_ns() - idle_since > p.timeout_ns) {
+            set_error(p.dev.err, EP_ERR_TIMEOUT);
+            break;
+        }
+        __nanosleep(sleep);
+        sleep = min(sleep * 2u, 256u);
+    }
+}
 
-__device__ void consumer_warp(const DispatchParams &p, int c, long long expected) {
+// ------------------------------------------------------ channel CTA: poster
+
+// A ring slot holds one TransferCmd packed into two 64-bit words, each tagged
+// with the slot's lap (command index / D, as 1..65535 in 16 bits).  Every offset of a
+// command is a whole number of rows, so the words carry rows, not bytes:
+//   w0 = lap:16 | dst_rank:6 | rows:11 | src_row:31   (src_offset = src_row * B, size = rows * B)
+//   w1 = lap:16 | 0:17       | dst_row:31             (dst_offset = dst_row * B)
+// A 64-bit access is single-copy atomic, so a consumer that finds both tags
+// equal to the lap it expects has the whole record of this lap.
+__device__ __forceinline__ unsigned long long lap_tag(unsigned long long idx, int lg_depth) {
+    // 1..65535: consecutive laps of a slot differ and no lap reads as the
+    // zeroed slots of a fresh ring
+    return (((idx >> lg_depth) % 65535ull) + 1ull) << 48;
+}
+
+// Per-lane ring statistics, reduced once at the end of the kernel.
+struct LaneStats {
+    unsigned long long batches = 0, stalls = 0;
+    unsigned max_batch = 0, max_inflight = 0;
+};
+
+// Pair tables (num_tokens_per_rank, recv_off, send_off; [R, R] each), staged
+// in a channel CTA's shared memory so that turning a notice into commands
+// costs no round trip.
+struct PairTables {
+    const int *cnt, *recv0, *send0;
+};
+
+// The posters of ring c (kPosterWarps warps; warp w takes chunk groups
+// w, w + kPosterWarps, ... of 32 chunks, lane i chunk 32 * group + i).  A
+// lane waits for its chunk's ready flag, loads the chunk's notice for every
+// destination of ring c at once, and derives the messages the chunk
+// completes: those of pair (s, d) whose last row lies in the chunk's rows
+// [jlo, jhi] of the pair -- all earlier rows of the pair are in earlier
+// chunks.  It then reserves its batches (up to kMaxResv atomicAdds on head in
+// flight, each of up to `batch` commands) and publishes each batch as soon as
+// base + n - retired <= max_inflight, retired being the poller's retire point
+// read from shared memory.  The warp loops until every lane is through; a
+// lane never waits on another lane's batch.
+constexpr int kPosterWarps = 4;
+constexpr int kMaxResv = 4;
+
+__device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long long *words, const PairTables &pt,
+                            unsigned long long *ring) {
     const int lane = threadIdx.x & 31;
-    unsigned long long *tail = p.dev.tail + static_cast<int64_t>(c) * kHeadStride;
-    const unsigned long long base = ld_relaxed(tail);
+    const int R = p.R, C = p.C, G = p.G;
+    const int nd = c < R ? (R - 1 - c) / C + 1 : 0;   // destinations d = c, c + C, ... on this ring
+    const unsigned long long dmask = static_cast<unsigned long long>(p.D - 1);
+    const unsigned long long limit = static_cast<unsigned long long>(p.max_inflight);
+    const unsigned int tag = static_cast<unsigned int>(words[kWGen]) + 1u;
+    unsigned long long *head = &words[kWHead];
+    LaneStats st;
+    bool failed = false;
+    const int ngroups = (p.nchunks + 31) / 32;
+    int gb[kMaxRanks], ge[kMaxRanks];   // this lane's messages [gb, ge) per destination index
+    for (int grp = w; grp < ngroups && !failed; grp += kPosterWarps) {
+        const int k = grp * 32 + lane;
+        const int s = k < p.nchunks ? k / p.chunks_per_rank : 0;
+        // 0: wait for the chunk; 1: reserve; 2: publish; 3: done
+        int phase = (k < p.nchunks && nd > 0) ? 0 : 3;
+        int total = 0, next_res = 0, nres = 0, q = 0, ci = 0, cg = 0;
+        unsigned long long base[kMaxResv];
+        int nn[kMaxResv];
+        uint64_t t0 = globaltimer_ns();
+        unsigned sleep = 32;
+        while (true) {
+            bool progress = false;
+            if (phase == 0 && ld_acquire_u32(p.dev.ready + k) == tag) {
+                const int32_t *nt = p.dev.notice + static_cast<int64_t>(k) * 2 * R;
+                bool bad = false;
+                for (int i = 0; i < nd; ++i) {
+                    const int d = c + i * C;
+                    const int2 lh = __ldcg(reinterpret_cast<const int2 *>(nt + 2 * d));
+                    gb[i] = ge[i] = 0;
+                    if (lh.y < 0) continue;
+                    const int cnt = pt.cnt[s * R + d], r0 = pt.recv0[s * R + d];
+                    const int jlo = lh.x - r0, jhi = lh.y - r0;
+                    if (jlo < 0 || jhi < jlo || jhi >= cnt) {
+                        bad = true;
+                        continue;
+                    }
+                    gb[i] = jlo / G;
+                    ge[i] = max(gb[i], (jhi == cnt - 1) ? (cnt - 1) / G + 1 : (jhi + 1) / G);
+                    total += ge[i] - gb[i];
+                }
+                if (bad) {
+                    set_error(p.dev.err, EP_ERR_INVALID_ARG);
+                    phase = 3;
+                } else {
+                    phase = total > 0 ? 1 : 3;
+                    ci = 0;
+                    cg = gb[0];
+                }
+                progress = true;
+            }
+            if (phase == 1) {
+                const int nb = (total + p.batch - 1) / p.batch;
+                nres = min(kMaxResv, nb - next_res);
+#pragma unroll
+                for (int j = 0; j < kMaxResv; ++j) {
+                    if (j >= nres) break;
+                    nn[j] = min(p.batch, total - (next_res + j) * p.batch);
+                    base[j] = atomicAdd(head, static_cast<unsigned long long>(nn[j]));
+                }
+                next_res += nres;
+                q = 0;
+                phase = 2;
+                progress = true;
+            }
+            if (phase == 2) {
+                const unsigned long long retired = ld_acquire_cta_shared(&words[kWProgress]);
+                while (q < nres) {
+                    const int n = nn[q];
+                    const unsigned long long b0 = base[q];
+                    if (b0 + n - retired > limit) {
+                        ++st.stalls;
+                        break;
+                    }
+                    for (int i = 0; i < n; ++i) {
+                        while (cg >= ge[ci]) {   // next destination with messages
+                            ++ci;
+                            cg = gb[ci];
+                        }
+                        const int d = c + ci * C;
+                        const int j0 = cg * G;
+                        const int rows = min(G, pt.cnt[s * R + d] - j0);
+                        const unsigned long long w0 = (static_cast<unsigned long long>(d) << 42) |
+                                                      (static_cast<unsigned long long>(rows) << 31) |
+                                                      (static_cast<unsigned long long>(pt.send0[s * R + d] + j0) & 0x7FFFFFFFull);
+                        const unsigned long long w1 = static_cast<unsigned long long>(pt.recv0[s * R + d] + j0) & 0x7FFFFFFFull;
+                        const unsigned long long idx = b0 + i;
+                        const unsigned long long lt = lap_tag(idx, p.lg_depth);
+                        st_shared_v2(ring + 2 * (idx & dmask), w0 | lt, w1 | lt);
+                        ++cg;
+                    }
+                    st.batches += 1;
+                    st.max_batch = max(st.max_batch, static_cast<unsigned>(n));
+                    st.max_inflight = max(st.max_inflight, static_cast<unsigned>(b0 + n - retired));
+                    ++q;
+                    progress = true;
+                }
+                if (q == nres) phase = next_res * p.batch < total ? 1 : 3;
+            }
+            if (!__any_sync(kFull, phase < 3)) break;
+            if (__any_sync(kFull, progress)) {
+                if (progress) {
+                    t0 = globaltimer_ns();
+                    sleep = 32;
+                }
+                continue;
+            }
+            bool give_up = false;
+            if (phase < 3) {
+                if (read_error(p.dev.err) != 0) {
+                    give_up = true;
+                } else if (globaltimer_ns() - t0 > p.timeout_ns) {
+                    set_error(p.dev.err, EP_ERR_TIMEOUT);
+                    give_up = true;
+                }
+            }
+            if (__any_sync(kFull, give_up)) {
+                failed = true;
+                break;
+            }
+            // lanes waiting on a chunk poll device memory: back off to a few
+            // microseconds (a chunk takes tens); lanes waiting on the ring
+            // poll shared memory: stay quick
+            const unsigned cap = __any_sync(kFull, phase == 2) ? 128u : 4096u;
+            __nanosleep(sleep);
+            sleep = min(sleep * 2u, cap);
+        }
+    }
+    // statistics: one reduction per warp
+    unsigned long long b = st.batches, sp = st.stalls;
+    unsigned mb = st.max_batch, mi = st.max_inflight;
+    for (int o = 16; o; o >>= 1) {
+        b += __shfl_xor_sync(kFull, b, o);
+        sp += __shfl_xor_sync(kFull, sp, o);
+        mb = max(mb, __shfl_xor_sync(kFull, mb, o));
+        mi = max(mi, __shfl_xor_sync(kFull, mi, o));
+    }
+    if (lane == 0 && b) {
+        RingStatsDev *stt = p.dev.stats + c;
+        atomicAdd(&stt->batches, b);
+        atomicMax(&stt->max_batch, mb);
+        atomicMax(&stt->max_inflight, mi);
+        if (sp) atomicAdd(&stt->stall_polls, sp);
+    }
+}
+
+// ------------------------------------------------------ channel CTA: poller
+// Takes the longest run of published slots from the tail, copies the packed
+// records into a shared staging ring for the logger, and moves the ring's
+// tail (the retire point) in shared memory -- the posters read it there, so
+// flow control costs no round trip.  Having no global stores of its own, its
+// release on the tail waits on nothing slow.
+__device__ void consumer_poll(const DispatchParams &p, long long expected, unsigned long long *words,
+                              const unsigned long long *ring, unsigned long long *stage) {
+    const int lane = threadIdx.x & 31;
+    const unsigned long long base = words[kWBase];
     const unsigned long long end = base + static_cast<unsigned long long>(expected);
-    // every slot that can be outstanding (max_inflight), polled drain_batch at a time
     int window = max(p.drain_batch, ((p.max_inflight + 31) / 32) * 32);
     window = min(window, 32 * kMaxPollRounds);
     const unsigned long long dmask = static_cast<unsigned long long>(p.D - 1);
-    const int64_t ring0 = static_cast<int64_t>(c) * p.D;
     unsigned long long pos = base;
     uint64_t idle_since = globaltimer_ns();
     unsigned sleep = 32;
     while (pos < end) {
         const int avail = static_cast<int>(min(end - pos, static_cast<unsigned long long>(window)));
-        const int rounds = (avail + 31) / 32;
-        // all status loads of the step in flight together
+        ulonglong2 v[kMaxPollRounds];
         bool pub[kMaxPollRounds];
 #pragma unroll
         for (int q = 0; q < kMaxPollRounds; ++q) {
             pub[q] = false;
+            v[q] = make_ulonglong2(0ull, 0ull);
             const int off = q * 32 + lane;
-            if (q < rounds && off < avail) {
+            if (off < avail) {
                 const unsigned long long idx = pos + static_cast<unsigned long long>(off);
-                pub[q] = ld_acquire(p.dev.status + ring0 + static_cast<int64_t>(idx & dmask)) == 2ull * idx + 1ull;
+                v[q] = ld_shared_v2(ring + 2 * (idx & dmask));
+                const unsigned long long lt = lap_tag(idx, p.lg_depth);
+                pub[q] = (v[q].x & 0xFFFF000000000000ull) == lt && (v[q].y & 0xFFFF000000000000ull) == lt;
             }
         }
-        // the longest run of published slots from pos
         int ready = 0;
 #pragma unroll
         for (int q = 0; q < kMaxPollRounds; ++q) {
-            if (q >= rounds || ready < q * 32) break;
+            if (ready < q * 32) break;
             const unsigned bal = __ballot_sync(kFull, pub[q]);
             ready += bal == kFull ? 32 : __ffs(~bal) - 1;
         }
+        // room in the staging ring (the logger frees it as it writes the log)
+        if (ready > 0 && pos + ready - ld_acquire_cta_shared(&words[kWLogged]) > kLogStage) ready = 0;
         if (ready > 0) {
 #pragma unroll
             for (int q = 0; q < kMaxPollRounds; ++q) {
                 const int off = q * 32 + lane;
                 if (off < ready) {
-                    const unsigned long long idx = pos + static_cast<unsigned long long>(off);
-                    const int64_t sidx = ring0 + static_cast<int64_t>(idx & dmask);
-                    const uint4 *src = reinterpret_cast<const uint4 *>(p.dev.slots + sidx);
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.dev.log + static_cast<int64_t>(c) * p.log_cap +
-                                                           static_cast<int64_t>(idx - base));
-                    const uint4 a = __ldcg(src), b = __ldcg(src + 1);
-                    dst[0] = a;
-                    dst[1] = b;
-                    st_relaxed(p.dev.status + sidx, 2ull * idx + 2ull);   // COMPLETED
+                    const unsigned long long i = (pos - base + off) & (kLogStage - 1);
+                    st_shared_v2(stage + 2 * i, v[q].x, v[q].y);
                 }
             }
             pos += static_cast<unsigned long long>(ready);
             __syncwarp();
-            if (lane == 0) st_release(tail, pos);
+            if (lane == 0) st_release_cta_shared(&words[kWProgress], pos);   // slots read, records staged
             idle_since = globaltimer_ns();
             sleep = 32;
         } else {
@@ -540,43 +641,118 @@ __device__ void consumer_warp(const DispatchParams &p, int c, long long expected
                 break;
             }
             __nanosleep(sleep);
-            sleep = min(sleep * 2u, 256u);
+            sleep = min(sleep * 2u, 128u);
         }
     }
-    if (lane == 0) p.dev.log_count[c] = static_cast<int64_t>(pos - base);
+    __syncwarp();
+    if (lane == 0) st_release_cta_shared(&words[kWStopped], 1ull);
+}
+
+// ------------------------------------------------------ channel CTA: logger
+// Decodes staged records into TransferCmds, appends them to the channel's log
+// in device memory, and publishes the ring's cumulative tail (and, at the end,
+// head) to device memory with release stores, for the host and the next call.
+__device__ void consumer_log(const DispatchParams &p, int c, long long expected, unsigned long long *words,
+                             const unsigned long long *stage) {
+    const int lane = threadIdx.x & 31;
+    unsigned long long *tail = p.dev.tail + static_cast<int64_t>(c) * kHeadStride;
+    const unsigned long long base = words[kWBase];
+    const unsigned long long end = base + static_cast<unsigned long long>(expected);
+    const int64_t B = p.row_bytes;
+    ep_transfer_cmd *log = p.dev.log + static_cast<int64_t>(c) * p.log_cap;
+    unsigned long long logged = base;
+    uint64_t idle_since = globaltimer_ns();
+    while (logged < end) {
+        const unsigned long long cur = ld_acquire_cta_shared(&words[kWProgress]);
+        if (cur > logged) {
+            for (unsigned long long j = logged + lane; j < cur; j += 32) {
+                const unsigned long long i = (j - base) & (kLogStage - 1);
+                const ulonglong2 w = ld_shared_v2(stage + 2 * i);
+                const uint32_t d = static_cast<uint32_t>((w.x >> 42) & 63ull);
+                const uint32_t rows = static_cast<uint32_t>((w.x >> 31) & 2047ull);
+                const uint64_t src = (w.x & 0x7FFFFFFFull) * static_cast<uint64_t>(B);
+                const uint64_t dst = (w.y & 0x7FFFFFFFull) * static_cast<uint64_t>(B);
+                uint4 *o = reinterpret_cast<uint4 *>(log + (j - base));
+                o[0] = make_uint4(d, rows * static_cast<uint32_t>(B), static_cast<uint32_t>(src),
+                                  static_cast<uint32_t>(src >> 32));
+                o[1] = make_uint4(static_cast<uint32_t>(dst), static_cast<uint32_t>(dst >> 32), 0u, 0u);
+            }
+            logged = cur;
+            __syncwarp();
+            if (lane == 0) {
+                st_release_cta_shared(&words[kWLogged], logged);   // staging entries free again
+                st_release(tail, logged);
+            }
+            idle_since = globaltimer_ns();
+            continue;
+        }
+        if (ld_acquire_cta_shared(&words[kWStopped]) != 0ull &&
+            ld_acquire_cta_shared(&words[kWProgress]) == logged)   // the poller stopped early
+            break;
+        if (globaltimer_ns() - idle_since > 2 * p.timeout_ns) {
+            set_error(p.dev.err, EP_ERR_TIMEOUT);
+            break;
+        }
+        __nanosleep(64);
+    }
+    __syncwarp();
+    if (lane == 0) {
+        p.dev.log_count[c] = static_cast<int64_t>(logged - base);
+        // every command of the call has been reserved once all were retired
+        st_release(p.dev.head + static_cast<int64_t>(c) * kHeadStride, atomicAdd(&words[kWHead], 0ull));
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    const SmemLayout L(p.R, p.C, p.stage_bytes, p.stages, p.meta_slots);
-    int *scratch = reinterpret_cast<int *>(smem + L.scratch_off);
-    int *flags = scratch + 3 * p.R + 2 * p.C + 1;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
-    uint64_t *bar_full = bars, *meta_full = bars + p.stages, *chunk_done = meta_full + p.meta_slots;
+    const SmemLayout L(p.R, p.D, p.stage_bytes, p.stages);
+    int *rbase = reinterpret_cast<int *>(smem + L.scratch_off);
+    unsigned long long *words =
+        reinterpret_cast<unsigned long long *>(smem + L.scratch_off + ((p.R + 3) & ~3) * 4);
+    uint64_t *b = reinterpret_cast<uint64_t *>(smem + L.bar_off);
+    Bars bars;
+    bars.stage_full = b;
+    bars.meta_full = b + p.stages;
+    bars.meta_free = bars.meta_full + kMetaSlots;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool channel_cta = static_cast<int>(blockIdx.x) < p.C;
+    const int qcta = static_cast<int>(blockIdx.x) - p.C, NQ = static_cast<int>(gridDim.x) - p.C;
 
     // Prologue: barriers, window starts, and the checks every CTA takes alike
     // so that either all of them run or none does.
-    if (warp == kCopyWarp && lane == 0) {
-        for (int i = 0; i < p.stages; ++i) mbar_init(&bar_full[i], 1);
-        for (int i = 0; i < p.meta_slots; ++i) {
-            mbar_init(&meta_full[i], 1);
-            mbar_init(&chunk_done[i], 1);
+    if (warp == 0 && lane == 0) {
+        if (!channel_cta) {
+            for (int i = 0; i < p.stages; ++i) mbar_init(&bars.stage_full[i], 1);
+            for (int i = 0; i < kMetaSlots; ++i) {
+                mbar_init(&bars.meta_full[i], 1);
+                mbar_init(&bars.meta_free[i], 1);
+            }
+            mbar_fence_init();
         }
-        mbar_fence_init();
+        words[kWProgress] = 0ull;
+        words[kWStopped] = 0ull;
+        words[kWGen] = ld_relaxed_u32(p.dev.disp_gen);
+        if (channel_cta) {
+            // the ring is drained between calls, so tail is where this call starts
+            const unsigned long long base = ld_relaxed(p.dev.tail + static_cast<int64_t>(blockIdx.x) * kHeadStride);
+            words[kWBase] = base;
+            words[kWProgress] = base;
+            words[kWHead] = base;
+            words[kWLogged] = base;
+        }
     }
-    long long my_expected = 0;
-    if (warp == kMetaWarp) {
-        for (int d = lane; d < p.R; d += 32) scratch[d] = __ldg(p.recv_base + d);
+    if (warp == 1) {
+        for (int d = lane; d < p.R; d += 32) rbase[d] = __ldg(p.recv_base + d);
         // N against the receive capacity; every channel's count against its log
         const long long n_recv = static_cast<long long>(__ldg(p.recv_base + p.R - 1)) + __ldg(p.recv_count + p.R - 1);
-        long long worst = 0;
+        long long worst = 0, mine = 0;
         for (int c = 0; c < p.C; ++c) {
             long long part = 0;
             for (int i = lane; i < p.R * p.R; i += 32)
                 if ((i % p.R) % p.C == c) part += __ldg(p.msg_count + i);
             for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
             worst = max(worst, part);
+            if (channel_cta && c == static_cast<int>(blockIdx.x)) mine = part;
         }
         if (lane == 0) {
             int abort = read_error(p.dev.err) != 0;
@@ -588,33 +764,71 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
                 set_error(p.dev.err, EP_ERR_INVALID_ARG);
                 abort = 1;
             }
-            flags[0] = abort;
+            words[kWAbort] = static_cast<unsigned long long>(abort);
+            words[kWExpected] = static_cast<unsigned long long>(mine);
         }
     }
-    if (warp == kConsumerWarp && static_cast<int>(blockIdx.x) < p.C) {
-        const int c = blockIdx.x;
-        long long part = 0;
-        for (int i = lane; i < p.R * p.R; i += 32)
-            if ((i % p.R) % p.C == c) part += __ldg(p.msg_count + i);
-        for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
-        my_expected = part;
+    if (channel_cta) {
+        // the ring: tags are laps of the cumulative index, so clear the slots
+        // (a fresh launch's shared memory holds anything)
+        unsigned long long *ring = reinterpret_cast<unsigned long long *>(smem + SmemLayout::ring_off(p.R));
+        for (int i = threadIdx.x; i < 2 * p.D; i += blockDim.x) ring[i] = 0ull;
+        int *tab = reinterpret_cast<int *>(smem);
+        const int RR = p.R * p.R;
+        for (int i = threadIdx.x; i < RR; i += blockDim.x) {
+            tab[i] = __ldg(p.cnt + i);
+            tab[RR + i] = __ldg(p.recv_off + i);
+            tab[2 * RR + i] = __ldg(p.send_off + i);
+        }
     }
     __syncthreads();
-    if (flags[0]) return;
+    const long long expected = static_cast<long long>(words[kWExpected]);
 
-    if (warp == kCopyWarp) {
-        copy_warp(p, smem, L, bar_full, meta_full, chunk_done);
-    } else if (warp == kMetaWarp) {
-        meta_warp(p, smem, L, meta_full, chunk_done, scratch);
-    } else if (static_cast<int>(blockIdx.x) < p.C && !(p.debug & EP_DEBUG_DISABLE_CONSUMER)) {
-        consumer_warp(p, blockIdx.x, my_expected);
+    if (words[kWAbort] == 0ull) {
+        if (channel_cta) {
+            const int c = blockIdx.x;
+            if (warp < kPosterWarps) {
+                PairTables pt;
+                pt.cnt = reinterpret_cast<const int *>(smem);
+                pt.recv0 = pt.cnt + p.R * p.R;
+                pt.send0 = pt.recv0 + p.R * p.R;
+                poster_warp(p, c, warp, words, pt,
+                            reinterpret_cast<unsigned long long *>(smem + SmemLayout::ring_off(p.R)));
+            } else if (!(p.debug & EP_DEBUG_DISABLE_CONSUMER)) {
+                unsigned long long *ring = reinterpret_cast<unsigned long long *>(smem + SmemLayout::ring_off(p.R));
+                unsigned long long *stage = ring + 2 * p.D;
+                if (warp == kPosterWarps)
+                    consumer_poll(p, expected, words, ring, stage);
+                else
+                    consumer_log(p, c, expected, words, stage);
+            }
+        } else {
+            if (warp == 0)
+                copy_warp(p, smem, L, bars, qcta, NQ, words);
+            else if (warp == 1)
+                meta_warp(p, smem, L, bars, rbase, qcta, NQ);
+            else if (warp == 2)
+                notify_warp(p, qcta, NQ, words);
+        }
+    }
+
+    // Epilogue: the last CTA out advances the dispatch generation (which tags
+    // the chunks' ready flags) and re-arms the counter for the next call.
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.dev.disp_done, 1u) == gridDim.x - 1) {
+            *p.dev.disp_done = 0u;
+            atomicAdd(p.dev.disp_gen, 1u);
+        }
     }
 }
 
 }  // namespace
 
-// Geometry: one CTA per SM; stages sized so that a stage holds a run of whole
-// rows (rows <= 16 KB) or one piece of a row, and as many stages as fit.
+// Geometry: one CTA per SM (C channel CTAs, the rest copy CTAs); stages sized
+// so that a stage holds a run of whole rows (rows <= 16 KB) or one piece of a
+// row, and as many stages as fit.
 ep_status plan_dispatch(ep_ctx *h) {
     const int R = h->cfg.num_ranks, C = h->cfg.channels;
     const int64_t B = 2ll * h->cfg.hidden;
@@ -629,28 +843,28 @@ ep_status plan_dispatch(ep_ctx *h) {
         piece_bytes = static_cast<int>(((B + pieces - 1) / pieces + 15) / 16 * 16);
     }
     const int stage_bytes = ((rows_per_item * piece_bytes) + 127) / 128 * 128;
-    const int meta_slots = 3;
     int max_smem = 0;
     if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device) != cudaSuccess)
         return EP_ERR_CUDA;
     const int reserve = 1024;   // static + alignment slack
     int stages = 0;
     for (int s = 15; s >= 3; --s) {
-        SmemLayout L(R, C, stage_bytes, s, meta_slots);
+        SmemLayout L(R, h->cfg.ring_depth, stage_bytes, s);
         if (L.total + reserve <= max_smem) {
             stages = s;
             break;
         }
     }
     if (stages == 0) return EP_ERR_INVALID_ARG;
-    SmemLayout L(R, C, stage_bytes, stages, meta_slots);
+    SmemLayout L(R, h->cfg.ring_depth, stage_bytes, stages);
     h->rows_per_item = rows_per_item;
     h->pieces = pieces;
     h->piece_bytes = piece_bytes;
     h->stage_bytes = stage_bytes;
     h->stages = stages;
-    h->prefetch = stages / 2;
-    h->meta_slots = meta_slots;
+    h->prefetch = kPrefetchItems < stages - 1 ? kPrefetchItems : stages - 1;
+    h->store_lag = kStoreLagItems < stages - h->prefetch ? kStoreLagItems : stages - h->prefetch;
+    h->meta_slots = kMetaSlots;
     h->disp_smem = static_cast<size_t>(L.total);
     h->disp_threads = kThreads;
     h->chunks_per_rank = (h->cfg.tokens_per_rank + kChunkTokens - 1) / kChunkTokens;
@@ -663,8 +877,8 @@ ep_status plan_dispatch(ep_ctx *h) {
             cudaSuccess ||
         per_sm < 1)
         return EP_ERR_CUDA;
-    h->disp_grid = h->sm_count * 1;
-    if (h->disp_grid < C) return EP_ERR_INVALID_ARG;
+    h->disp_grid = h->sm_count;
+    if (h->disp_grid < C + 1) return EP_ERR_INVALID_ARG;   // at least one copy CTA
     return EP_OK;
 }
 
@@ -703,9 +917,10 @@ ep_status launch_dispatch(ep_ctx *h, const void *x, const ep_layout_out *lay, vo
     p.stage_bytes = h->stage_bytes;
     p.stages = h->stages;
     p.prefetch = h->prefetch;
+    p.store_lag = h->store_lag;
     p.meta_slots = h->meta_slots;
-    p.msgs_per_pair = h->msgs_per_pair;
     p.slot_vec = (p.R % 4 == 0 && reinterpret_cast<uintptr_t>(lay->token_slot) % 16 == 0) ? 1 : 0;
+    p.lg_depth = __builtin_ctz(static_cast<unsigned>(p.D));
     void *args[] = {&p};
     const cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(dispatch_kernel),
                                                       dim3(h->disp_grid), dim3(kThreads), args, h->disp_smem, st);

@@ -41,14 +41,15 @@ struct DevState {
     int32_t *col_prefix;                // [(R + 1) * R] column prefix at each rank's first token
     int64_t *n_recv;                    // N of the last layout
     // rings
-    ep_transfer_cmd *slots;             // [C * D]
-    unsigned long long *status;         // [C * D] 2*idx+1 posted, 2*idx+2 retired
     unsigned long long *head;           // [C * kHeadStride]
     unsigned long long *tail;           // [C * kHeadStride]
     RingStatsDev *stats;                // [C]
     ep_transfer_cmd *log;               // [C * log_cap]
     int64_t *log_count;                 // [C]
-    unsigned int *msg_fill;             // [R * R * msgs_per_pair] rows landed per message (G > 1)
+    int32_t *notice;                    // [nchunks * 2R] per chunk: first/last window slot per rank
+    unsigned int *ready;                // [nchunks] = dispatch generation + 1 once the chunk's rows landed
+    unsigned int *disp_gen;             // dispatch calls so far (tags `ready`)
+    unsigned int *disp_done;            // CTAs finished in the current dispatch
 };
 
 // Layout kernel parameters.
@@ -80,8 +81,9 @@ struct DispatchParams {
     int piece_bytes;     // bytes per piece (a multiple of 16)
     int stage_bytes;     // bytes per shared-memory stage
     int stages, prefetch, meta_slots;
-    int msgs_per_pair;   // ceil(Tpr / G)
+    int store_lag;       // items whose bulk stores may be in flight
     int slot_vec;        // 1: token_slot rows are 16-byte aligned (int4 loads)
+    int lg_depth;        // log2(D)
 };
 
 // Combine kernel parameters.
@@ -113,9 +115,9 @@ struct ep_ctx {
     // dispatch geometry
     int disp_grid, disp_threads;
     size_t disp_smem;
-    int stage_bytes, stages, prefetch, meta_slots;
+    int stage_bytes, stages, prefetch, meta_slots, store_lag;
     int rows_per_item, pieces, piece_bytes;
-    int chunks_per_rank, nchunks, msgs_per_pair;
+    int chunks_per_rank, nchunks;
     int64_t log_cap;
     // combine geometry
     int comb_grid, comb_threads;
@@ -138,6 +140,9 @@ ep_status plan_combine(ep_ctx *h);
 // ------------------------------------------------------------ device helpers
 #ifdef __CUDACC__
 
+__device__ __forceinline__ uint32_t smem_u32_(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
 __device__ __forceinline__ void set_error(int32_t *err, int code) {
     atomicCAS(reinterpret_cast<int *>(err), 0, code);
 }
@@ -163,6 +168,44 @@ __device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long lon
 }
 __device__ __forceinline__ void st_release(unsigned long long *p, unsigned long long v) {
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned int ld_relaxed_u32(const unsigned int *p) {
+    unsigned int v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_u32(unsigned int *p, unsigned int v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ ulonglong2 ld_relaxed_v2(const unsigned long long *p) {
+    ulonglong2 v;
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_v2(unsigned long long *p, unsigned long long a, unsigned long long b) {
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+__device__ __forceinline__ ulonglong2 ld_shared_v2(const unsigned long long *p) {
+    ulonglong2 v;
+    asm volatile("ld.volatile.shared::cta.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "r"(smem_u32_(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_shared_v2(unsigned long long *p, unsigned long long a, unsigned long long b) {
+    asm volatile("st.volatile.shared::cta.v2.u64 [%0], {%1, %2};" ::"r"(smem_u32_(p)), "l"(a), "l"(b) : "memory");
+}
+__device__ __forceinline__ void st_release_cta_shared(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.release.cta.shared::cta.u64 [%0], %1;" ::"r"(smem_u32_(p)), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_cta_shared(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.cta.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(smem_u32_(p)) : "memory");
+    return v;
 }
 __device__ __forceinline__ void st_relaxed(unsigned long long *p, unsigned long long v) {
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");

@@ -236,7 +236,8 @@ ep_status ep_ring_stats_get(ep_handle h, ep_ring_stats *out, int32_t n);
 
 /* Completion query ([UCCL-EP] s2.2 CheckCompletion): EP_OK if command index
  * cmd_idx (cumulative since create/reset) of `channel` has been retired by its
- * consumer, EP_ERR_NOT_READY if not yet.  Synchronous device read. */
+ * consumer -- the channel's tail has passed it -- EP_ERR_NOT_READY if not yet.
+ * Synchronises the device, then reads the tail. */
 ep_status ep_check_completion(ep_handle h, int32_t channel, uint64_t cmd_idx);
 
 /* Launch parameters and allocation size of a handle.  Host only. */

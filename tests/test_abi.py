@@ -56,7 +56,7 @@ def test_defaults_are_the_tuning_table(ep, golden):
 @pytest.mark.parametrize("field,value", [
     ("num_ranks", 0), ("num_ranks", 65), ("tokens_per_rank", 0), ("hidden", 100), ("hidden", 0),
     ("num_experts", 250), ("topk", 0), ("topk", 33), ("channels", 0), ("channels", 65),
-    ("ring_depth", 1000), ("ring_depth", 4), ("max_inflight", 2048), ("max_inflight", 4), ("batch", 9),
+    ("ring_depth", 1000), ("ring_depth", 4), ("ring_depth", 16384), ("max_inflight", 2048), ("max_inflight", 4), ("batch", 9),
     ("batch", 0), ("rows_per_msg", -1), ("drain_batch", 48), ("drain_batch", 1024), ("debug_flags", 4),
 ])
 def test_invalid_configs_are_rejected_on_the_host(ep, field, value):
