@@ -143,6 +143,7 @@ ep_status ep_create(const ep_config *cfg, ep_handle *out) {
     const size_t o_ready = cv.take<unsigned int>(static_cast<size_t>(h->nchunks));
     const size_t o_gen = cv.take<unsigned int>(1);
     const size_t o_ddone = cv.take<unsigned int>(1);
+    const size_t o_cnext = cv.take<unsigned int>(1);
     h->alloc_bytes = cv.off;
     if (cudaMalloc(&h->alloc_base, h->alloc_bytes) != cudaSuccess) {
         delete h;
@@ -171,6 +172,7 @@ ep_status ep_create(const ep_config *cfg, ep_handle *out) {
     d.ready = reinterpret_cast<unsigned int *>(b + o_ready);
     d.disp_gen = reinterpret_cast<unsigned int *>(b + o_gen);
     d.disp_done = reinterpret_cast<unsigned int *>(b + o_ddone);
+    d.chunk_next = reinterpret_cast<unsigned int *>(b + o_cnext);
     if (cudaDeviceSynchronize() != cudaSuccess) {
         cudaFree(h->alloc_base);
         delete h;

@@ -18,8 +18,8 @@
 // How: one persistent cooperative kernel, one CTA per SM, in two kinds.
 //
 // Copy CTAs (all but the first C) move the rows.  Chunks of 32 tokens of one
-// source rank are dealt to them round-robin; three warps hand each chunk on
-// through mbarriers and shared counters:
+// source rank are drawn from a device-wide counter (so faster SMs take more);
+// three warps hand each chunk on through mbarriers and shared counters:
 //   copy    1-D TMA bulk loads of token rows (a run of whole rows when they
 //           are small, a piece of one row when it is large) into a ring of
 //           shared-memory stages, then one TMA bulk store per (row,
@@ -76,21 +76,39 @@ constexpr int kPrefetchItems = 4;   // row loads in flight per copy CTA
 constexpr int kStoreLagItems = 2;   // items whose stores may still be in flight
 constexpr int kMaxPollRounds = 16;  // up to 512 slots examined per consumer step
 constexpr int kLogStage = 1024;     // staged records (16 bytes each) awaiting the logger
+constexpr uint64_t kErrCheckNs = 20000;   // idle loops read the device error word this often
+constexpr int kPosterWarpsMax = 4;        // shared-memory room for this many poster warps
+
+// Shared words (u64) after rbase: abort flag; chunks complete (copy CTA) or
+// ring tail = retire point (channel CTA); poller stopped; ring base; dispatch
+// generation; messages expected on the channel; ring head; records logged;
+// chunk ids drawn (copy CTA); chunks stored in all, once known (copy CTA).
+// Then, in copy CTAs, the drawn chunk ids (a ring of kIdSlots ints).
+enum {
+    kWAbort = 0, kWProgress = 1, kWStopped = 2, kWBase = 3, kWGen = 4, kWExpected = 5, kWHead = 6, kWLogged = 7,
+    kWIds = 8, kWCopyDone = 9
+};
+constexpr int kNumWords = 10;
+constexpr int kIdSlots = 32;   // chunk ids a copy CTA has drawn but not yet retired
 
 // Shared-memory carve, identical on host and device.
 struct SmemLayout {
     int stage_off, meta_off, meta_slot_bytes, scratch_off, bar_off, total;
     __host__ __device__ static int ring_off(int R) { return ((12 * R * R) + 127) / 128 * 128; }
-    __host__ __device__ SmemLayout(int R, int D, int stage_bytes, int stages) {
+    // poster ranges: per poster warp, 32 chunks x ceil(R/C) int2, then 32 totals
+    __host__ __device__ static int ranges_off(int R, int D) { return ring_off(R) + 16 * D + 16 * kLogStage; }
+    __host__ __device__ static int ranges_bytes_per_warp(int R, int C) { return 32 * ((R + C - 1) / C) * 8 + 33 * 4 + 12; }
+    __host__ __device__ SmemLayout(int R, int C, int D, int stage_bytes, int stages) {
         stage_off = 0;
         // channel CTAs keep the pair tables (3 x R x R ints) and their ring
         // (D slots of 16 bytes) where copy CTAs keep their stages
-        const int stage_area = stage_bytes * stages, channel = ring_off(R) + 16 * D + 16 * kLogStage;
+        const int stage_area = stage_bytes * stages,
+                  channel = ranges_off(R, D) + kPosterWarpsMax * ranges_bytes_per_warp(R, C);
         meta_off = stage_area > channel ? stage_area : channel;
         meta_slot_bytes = ((32 * R + 33) + 3) / 4 * 16;   // dst[32*R] | pref[33]
         scratch_off = meta_off + meta_slot_bytes * kMetaSlots;
-        // scratch: rbase[R] ints, then 8 u64 words (flags, progress counters)
-        bar_off = (scratch_off + ((R + 3) & ~3) * 4 + 64 + 15) & ~15;
+        // scratch: rbase[R] ints, kNumWords u64 words, kIdSlots ints
+        bar_off = (scratch_off + ((R + 3) & ~3) * 4 + 8 * kNumWords + 4 * kIdSlots + 15) & ~15;
         total = bar_off + 8 * (stages + 2 * kMetaSlots);
     }
 };
@@ -103,10 +121,6 @@ struct MetaSlot {
     }
 };
 
-// Shared words (u64) after rbase: abort flag; chunks complete (copy CTA) or
-// ring tail = retire point (channel CTA); poller stopped; ring base; dispatch
-// generation; messages expected on the channel; ring head; records logged.
-enum { kWAbort = 0, kWProgress = 1, kWStopped = 2, kWBase = 3, kWGen = 4, kWExpected = 5, kWHead = 6, kWLogged = 7 };
 
 __device__ __forceinline__ int chunk_ntok(const DispatchParams &p, int k) {
     const int ci = k % p.chunks_per_rank;
@@ -119,41 +133,24 @@ __device__ __forceinline__ int64_t chunk_tok0(const DispatchParams &p, int k) {
 __device__ __forceinline__ int chunk_items(const DispatchParams &p, int ntok) {
     return p.pieces > 1 ? ntok * p.pieces : (ntok + p.rows_per_item - 1) / p.rows_per_item;
 }
-// Copy CTA q of NQ takes chunks q, q + NQ, ...
-__device__ __forceinline__ int my_chunks(const DispatchParams &p, int q, int NQ) {
-    return q < p.nchunks ? (p.nchunks - q + NQ - 1) / NQ : 0;
-}
-
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const DispatchParams &p) {
     return __all_sync(kFull, mbar_wait_bounded(bar, parity, p.dev.err, p.timeout_ns));
 }
 
-// Walks a copy CTA's items: chunks q, q + NQ, ...; items within each.
+// Walks the items of one chunk: a run of whole rows when they are small, a
+// piece of one row when it is large.  k < 0 marks the end of the chunks.
 struct ItemCursor {
-    int m, k, q, ntok, nitems, step;
-    bool valid;
-    __device__ void start(const DispatchParams &p, int first, int NQ) {
-        m = 0;
-        k = first;
-        step = NQ;
+    int k, q, ntok, nitems;
+    __device__ void set_chunk(const DispatchParams &p, int k_) {
+        k = k_;
         q = 0;
-        valid = k < p.nchunks;
-        if (valid) {
+        ntok = nitems = 0;
+        if (k >= 0) {
             ntok = chunk_ntok(p, k);
             nitems = chunk_items(p, ntok);
         }
     }
-    __device__ void advance(const DispatchParams &p) {
-        if (++q < nitems) return;
-        q = 0;
-        ++m;
-        k += step;
-        valid = k < p.nchunks;
-        if (valid) {
-            ntok = chunk_ntok(p, k);
-            nitems = chunk_items(p, ntok);
-        }
-    }
+    __device__ bool valid() const { return k >= 0; }
     // tokens [ta, tb) of the chunk, byte range [off, off + len) of each row
     __device__ void geometry(const DispatchParams &p, int &ta, int &tb, int &off, int &len) const {
         if (p.pieces > 1) {
@@ -175,20 +172,53 @@ struct Bars {
 };
 
 // ------------------------------------------------------------ copy CTA: copy
-__device__ void copy_warp(const DispatchParams &p, uint8_t *smem, const SmemLayout &L, const Bars &bars, int qcta,
-                          int NQ, unsigned long long *words) {
+// Chunks are drawn from a device-wide counter as the loads reach them, so
+// that CTAs on faster SMs take more chunks and all finish together; the ids
+// go to a shared ring for the meta and notify warps.
+__device__ void copy_warp(const DispatchParams &p, uint8_t *smem, const SmemLayout &L, const Bars &bars,
+                          unsigned long long *words, int *ids) {
     const int lane = threadIdx.x & 31;
     const int S = p.stages, P = p.prefetch;
     const int64_t B = p.row_bytes;
-    ItemCursor ld, stc;
-    ld.start(p, qcta, NQ);
-    stc.start(p, qcta, NQ);
     int64_t n_loaded = 0, n_stored = 0;
     int stored_chunks = 0, reported = 0;
     int64_t last_item[kDoneSlots];   // last item of chunks stored but not yet reported
 #pragma unroll
     for (int i = 0; i < kDoneSlots; ++i) last_item[i] = 0;
     bool ok = true;
+
+    // the next chunk id is drawn one chunk ahead so that its atomic's round
+    // trip overlaps a whole chunk of copying
+    unsigned int ahead = 0;
+    if (lane == 0) ahead = atomicAdd(p.dev.chunk_next, 1u);
+    int n_drawn = 0;
+    auto draw = [&]() -> int {   // warp-uniform
+        int k = -1;
+        if (lane == 0) {
+            k = ahead < static_cast<unsigned>(p.nchunks) ? static_cast<int>(ahead) : -1;
+            if (k >= 0) ahead = atomicAdd(p.dev.chunk_next, 1u);
+            ids[n_drawn % kIdSlots] = k;
+        }
+        k = __shfl_sync(kFull, k, 0);
+        ++n_drawn;
+        __syncwarp();
+        if (lane == 0) st_release_cta_shared(&words[kWIds], static_cast<unsigned long long>(n_drawn));
+        return k;
+    };
+    ItemCursor ld, stc;
+    int ld_m = 0, st_m = 0;
+    ld.set_chunk(p, draw());
+    stc.set_chunk(p, ld.k);
+    auto advance_ld = [&]() {
+        if (++ld.q < ld.nitems) return;
+        ++ld_m;
+        ld.set_chunk(p, draw());
+    };
+    auto advance_st = [&]() {
+        if (++stc.q < stc.nitems) return;
+        ++st_m;
+        stc.set_chunk(p, ids[st_m % kIdSlots]);   // drawn already: the loads run ahead
+    };
 
     auto issue_load = [&](const ItemCursor &c, int64_t idx) {
         if (lane == 0) {
@@ -214,15 +244,15 @@ __device__ void copy_warp(const DispatchParams &p, uint8_t *smem, const SmemLayo
         }
     };
 
-    for (int i = 0; i < P && ld.valid; ++i) {
+    for (int i = 0; i < P && ld.valid(); ++i) {
         issue_load(ld, n_loaded++);
-        ld.advance(p);
+        advance_ld();
     }
-    while (stc.valid) {
+    while (stc.valid()) {
         const int64_t i = n_stored;
-        const int slot = stc.m % kMetaSlots;
+        const int slot = st_m % kMetaSlots;
         if (stc.q == 0) {
-            const uint32_t par = static_cast<uint32_t>(stc.m / kMetaSlots) & 1u;
+            const uint32_t par = static_cast<uint32_t>(st_m / kMetaSlots) & 1u;
             if (!__all_sync(kFull, mbar_test(&bars.meta_full[slot], par))) {
                 // report what has landed before waiting on the meta warp
                 bulk_wait<0>();
@@ -259,19 +289,19 @@ __device__ void copy_warp(const DispatchParams &p, uint8_t *smem, const SmemLayo
             // every store of the chunk is issued: its destination list is free
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.meta_free[slot]);
-            last_item[stc.m % kDoneSlots] = i;
+            last_item[st_m % kDoneSlots] = i;
             ++stored_chunks;
         }
         ++n_stored;
-        stc.advance(p);
+        advance_st();
         // At most store_lag items' stores stay in flight; the stage of item
         // n_loaded was last used by item n_loaded - S, complete because
         // store_lag <= S - P.
         bulk_wait_n(p.store_lag);
         report_upto(n_stored - 1 - p.store_lag);
-        if (ld.valid) {
+        if (ld.valid()) {
             issue_load(ld, n_loaded++);
-            ld.advance(p);
+            advance_ld();
         }
     }
     bulk_wait<0>();
@@ -284,6 +314,10 @@ __device__ void copy_warp(const DispatchParams &p, uint8_t *smem, const SmemLayo
             mbar_wait_bounded(&bars.stage_full[j % S], static_cast<uint32_t>(j / S) & 1u, nullptr, p.timeout_ns);
         __syncwarp();
     }
+    // the id drawn ahead (if any) is simply unused: the counter only has to
+    // be reset between calls, which the last CTA does
+    if (lane == 0) st_release_cta_shared(&words[kWCopyDone], ok ? static_cast<unsigned long long>(stored_chunks) + 1ull
+                                                                : 1ull);
 }
 
 // ------------------------------------------------------------ copy CTA: meta
@@ -339,11 +373,25 @@ __device__ void build_meta(const DispatchParams &p, int k, const MetaSlot &ms, c
 }
 
 __device__ void meta_warp(const DispatchParams &p, uint8_t *smem, const SmemLayout &L, const Bars &bars,
-                          const int *rbase, int qcta, int NQ) {
+                          const int *rbase, unsigned long long *words, const int *ids) {
     const int lane = threadIdx.x & 31;
-    const int n_my = my_chunks(p, qcta, NQ);
-    for (int m = 0; m < n_my; ++m) {
-        const int k = qcta + m * NQ;
+    for (int m = 0;; ++m) {
+        // chunk id m, once the copy warp has drawn it
+        const uint64_t t0 = globaltimer_ns();
+        bool ok = true;
+        while (ld_acquire_cta_shared(&words[kWIds]) <= static_cast<unsigned long long>(m)) {
+            if (read_error(p.dev.err) != 0 || globaltimer_ns() - t0 > p.timeout_ns) {
+                ok = false;
+                break;
+            }
+            __nanosleep(64);
+        }
+        if (!__all_sync(kFull, ok)) {
+            set_error(p.dev.err, EP_ERR_TIMEOUT);
+            return;
+        }
+        const int k = ids[m % kIdSlots];
+        if (k < 0) return;
         if (m >= kMetaSlots &&
             !warp_wait(&bars.meta_free[m % kMetaSlots], static_cast<uint32_t>(m / kMetaSlots - 1) & 1u, p)) {
             set_error(p.dev.err, EP_ERR_TIMEOUT);
@@ -360,24 +408,24 @@ __device__ void meta_warp(const DispatchParams &p, uint8_t *smem, const SmemLayo
 // Sets ready[k] once chunk k's rows are complete: the copy warp counts
 // completed chunks in shared memory; one gpu-scope fence covers every chunk
 // reported since the last one.
-__device__ void notify_warp(const DispatchParams &p, int qcta, int NQ, unsigned long long *words) {
+__device__ void notify_warp(const DispatchParams &p, unsigned long long *words, const int *ids) {
     if ((threadIdx.x & 31) != 0) return;
-    const int n_my = my_chunks(p, qcta, NQ);
     const unsigned int tag = static_cast<unsigned int>(words[kWGen]) + 1u;
     int done = 0;
     uint64_t idle_since = globaltimer_ns();
     unsigned sleep = 32;
-    while (done < n_my) {
+    while (true) {
         const int now = static_cast<int>(ld_acquire_cta_shared(&words[kWProgress]));
         if (now > done) {
             fence_acq_rel_gpu();   // the chunks' rows are visible device-wide before their flags
-            for (int m = done; m < now; ++m)
-                st_relaxed_u32(p.dev.ready + qcta + static_cast<int64_t>(m) * NQ, tag);
+            for (int m = done; m < now; ++m) st_relaxed_u32(p.dev.ready + ids[m % kIdSlots], tag);
             done = now;
             idle_since = globaltimer_ns();
             sleep = 32;
             continue;
         }
+        const unsigned long long fin = ld_acquire_cta_shared(&words[kWCopyDone]);
+        if (fin != 0ull && static_cast<int>(ld_acquire_cta_shared(&words[kWProgress])) == done) break;
         if (read_error(p.dev.err) != 0) break;
         if (globaltimer_ns() - idle_since > p.timeout_ns) {
             set_error(p.dev.err, EP_ERR_TIMEOUT);
@@ -391,16 +439,17 @@ __device__ void notify_warp(const DispatchParams &p, int qcta, int NQ, unsigned 
 // ------------------------------------------------------ channel CTA: poster
 
 // A ring slot holds one TransferCmd packed into two 64-bit words, each tagged
-// with the slot's lap (command index / D, as 1..65535 in 16 bits).  Every offset of a
+// with the slot's lap (command index / D) in 16 bits.  Every offset of a
 // command is a whole number of rows, so the words carry rows, not bytes:
 //   w0 = lap:16 | dst_rank:6 | rows:11 | src_row:31   (src_offset = src_row * B, size = rows * B)
 //   w1 = lap:16 | 0:17       | dst_row:31             (dst_offset = dst_row * B)
 // A 64-bit access is single-copy atomic, so a consumer that finds both tags
 // equal to the lap it expects has the whole record of this lap.
 __device__ __forceinline__ unsigned long long lap_tag(unsigned long long idx, int lg_depth) {
-    // 1..65535: consecutive laps of a slot differ and no lap reads as the
-    // zeroed slots of a fresh ring
-    return (((idx >> lg_depth) % 65535ull) + 1ull) << 48;
+    // top bit set, low 15 bits of the lap: consecutive laps of a slot differ
+    // and no lap reads as the zeroed slots of a fresh ring
+    const unsigned lap = static_cast<unsigned>(idx >> lg_depth);
+    return static_cast<unsigned long long>(0x8000u | (lap & 0x7FFFu)) << 48;
 }
 
 // Per-lane ring statistics, reduced once at the end of the kernel.
@@ -416,149 +465,187 @@ struct PairTables {
     const int *cnt, *recv0, *send0;
 };
 
-// The posters of ring c (kPosterWarps warps; warp w takes chunk groups
-// w, w + kPosterWarps, ... of 32 chunks, lane i chunk 32 * group + i).  A
-// lane waits for its chunk's ready flag, loads the chunk's notice for every
-// destination of ring c at once, and derives the messages the chunk
-// completes: those of pair (s, d) whose last row lies in the chunk's rows
-// [jlo, jhi] of the pair -- all earlier rows of the pair are in earlier
-// chunks.  It then reserves its batches (up to kMaxResv atomicAdds on head in
-// flight, each of up to `batch` commands) and publishes each batch as soon as
-// base + n - retired <= max_inflight, retired being the poller's retire point
-// read from shared memory.  The warp loops until every lane is through; a
-// lane never waits on another lane's batch.
+// The posters of ring c.  Poster warp w takes chunk groups w, w + kPosterWarps,
+// ... of 32 chunks.  For a group it waits until every chunk is ready, then
+// lane i loads chunk 32 * group + i's notice for each destination of ring c
+// (one round trip for the group) and derives the messages the chunk
+// completes on ring c: those of pair (s, d) whose last row lies in the
+// chunk's rows [jlo, jhi] of the pair -- all earlier rows of the pair are in
+// earlier chunks.  The ranges go to shared memory.  Then the warp posts the
+// group's commands as one list, one command per lane and 32 a round: the
+// first lane of each batch of up to `batch` lanes reserves the batch's slots
+// with one atomicAdd on head, and each lane stores its slot as soon as
+// base + n - tail <= max_inflight (tail is the poller's retire point, in
+// shared memory).
 constexpr int kPosterWarps = 4;
-constexpr int kMaxResv = 4;
+// Channel-CTA warps: warps 3 and 5 are the poller and the logger; the others
+// post.  A warp's SM sub-partition is its index mod 4, so the poller (warp 3)
+// has one to itself and answers the posters without waiting for issue slots.
+constexpr int kPollWarp = 3, kLogWarp = 5;
+__device__ __forceinline__ int poster_index(int warp) { return warp < kPollWarp ? warp : warp - 1; }
 
 __device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long long *words, const PairTables &pt,
-                            unsigned long long *ring) {
+                            unsigned long long *ring, int2 *ranges, int *totals) {
     const int lane = threadIdx.x & 31;
     const int R = p.R, C = p.C, G = p.G;
     const int nd = c < R ? (R - 1 - c) / C + 1 : 0;   // destinations d = c, c + C, ... on this ring
+    const int ndmax = (R + C - 1) / C;
     const unsigned long long dmask = static_cast<unsigned long long>(p.D - 1);
     const unsigned long long limit = static_cast<unsigned long long>(p.max_inflight);
     const unsigned int tag = static_cast<unsigned int>(words[kWGen]) + 1u;
     unsigned long long *head = &words[kWHead];
+    const int rs = 32 - (32 % p.batch);               // commands per round: whole batches
+    const int leader = (lane / p.batch) * p.batch;    // first lane of this lane's batch
     LaneStats st;
     bool failed = false;
-    const int ngroups = (p.nchunks + 31) / 32;
-    int gb[kMaxRanks], ge[kMaxRanks];   // this lane's messages [gb, ge) per destination index
+    const int ngroups = nd > 0 ? (p.nchunks + 31) / 32 : 0;
+    uint64_t err_checked = globaltimer_ns();
     for (int grp = w; grp < ngroups && !failed; grp += kPosterWarps) {
         const int k = grp * 32 + lane;
-        const int s = k < p.nchunks ? k / p.chunks_per_rank : 0;
-        // 0: wait for the chunk; 1: reserve; 2: publish; 3: done
-        int phase = (k < p.nchunks && nd > 0) ? 0 : 3;
-        int total = 0, next_res = 0, nres = 0, q = 0, ci = 0, cg = 0;
-        unsigned long long base[kMaxResv];
-        int nn[kMaxResv];
-        uint64_t t0 = globaltimer_ns();
-        unsigned sleep = 32;
-        while (true) {
-            bool progress = false;
-            if (phase == 0 && ld_acquire_u32(p.dev.ready + k) == tag) {
+        // The group's chunks complete within a few microseconds of each other
+        // (they are drawn in order): wait for all of them, polling device
+        // memory with a back-off, before posting -- so that while posting
+        // the warp touches shared memory only and answers the ring at once.
+        {
+            bool rdy = k >= p.nchunks;
+            const uint64_t tw = globaltimer_ns();
+            unsigned nap = 256;
+            while (!__all_sync(kFull, rdy)) {
+                if (!rdy) rdy = ld_acquire_u32(p.dev.ready + k) == tag;
+                if (__all_sync(kFull, rdy)) break;
+                bool give_up = false;
+                if (!rdy && (read_error(p.dev.err) != 0 || globaltimer_ns() - tw > p.timeout_ns)) give_up = true;
+                if (__any_sync(kFull, give_up)) {
+                    if (read_error(p.dev.err) == 0) set_error(p.dev.err, EP_ERR_TIMEOUT);
+                    failed = true;
+                    break;
+                }
+                __nanosleep(nap);
+                nap = min(nap * 2u, 4096u);
+            }
+            if (failed) break;
+        }
+        // this lane's chunk: messages [gb, ge) per destination of ring c
+        {
+            int total = 0;
+            bool bad = false;
+            if (k < p.nchunks) {
+                const int s = k / p.chunks_per_rank;
                 const int32_t *nt = p.dev.notice + static_cast<int64_t>(k) * 2 * R;
-                bool bad = false;
                 for (int i = 0; i < nd; ++i) {
                     const int d = c + i * C;
                     const int2 lh = __ldcg(reinterpret_cast<const int2 *>(nt + 2 * d));
-                    gb[i] = ge[i] = 0;
-                    if (lh.y < 0) continue;
-                    const int cnt = pt.cnt[s * R + d], r0 = pt.recv0[s * R + d];
-                    const int jlo = lh.x - r0, jhi = lh.y - r0;
-                    if (jlo < 0 || jhi < jlo || jhi >= cnt) {
-                        bad = true;
-                        continue;
-                    }
-                    gb[i] = jlo / G;
-                    ge[i] = max(gb[i], (jhi == cnt - 1) ? (cnt - 1) / G + 1 : (jhi + 1) / G);
-                    total += ge[i] - gb[i];
-                }
-                if (bad) {
-                    set_error(p.dev.err, EP_ERR_INVALID_ARG);
-                    phase = 3;
-                } else {
-                    phase = total > 0 ? 1 : 3;
-                    ci = 0;
-                    cg = gb[0];
-                }
-                progress = true;
-            }
-            if (phase == 1) {
-                const int nb = (total + p.batch - 1) / p.batch;
-                nres = min(kMaxResv, nb - next_res);
-#pragma unroll
-                for (int j = 0; j < kMaxResv; ++j) {
-                    if (j >= nres) break;
-                    nn[j] = min(p.batch, total - (next_res + j) * p.batch);
-                    base[j] = atomicAdd(head, static_cast<unsigned long long>(nn[j]));
-                }
-                next_res += nres;
-                q = 0;
-                phase = 2;
-                progress = true;
-            }
-            if (phase == 2) {
-                const unsigned long long retired = ld_acquire_cta_shared(&words[kWProgress]);
-                while (q < nres) {
-                    const int n = nn[q];
-                    const unsigned long long b0 = base[q];
-                    if (b0 + n - retired > limit) {
-                        ++st.stalls;
-                        break;
-                    }
-                    for (int i = 0; i < n; ++i) {
-                        while (cg >= ge[ci]) {   // next destination with messages
-                            ++ci;
-                            cg = gb[ci];
+                    int gb = 0, ge = 0;
+                    if (lh.y >= 0) {
+                        const int cnt = pt.cnt[s * R + d], r0 = pt.recv0[s * R + d];
+                        const int jlo = lh.x - r0, jhi = lh.y - r0;
+                        if (jlo < 0 || jhi < jlo || jhi >= cnt) {
+                            bad = true;
+                        } else {
+                            gb = jlo / G;
+                            ge = max(gb, (jhi == cnt - 1) ? (cnt - 1) / G + 1 : (jhi + 1) / G);
                         }
-                        const int d = c + ci * C;
-                        const int j0 = cg * G;
-                        const int rows = min(G, pt.cnt[s * R + d] - j0);
-                        const unsigned long long w0 = (static_cast<unsigned long long>(d) << 42) |
-                                                      (static_cast<unsigned long long>(rows) << 31) |
-                                                      (static_cast<unsigned long long>(pt.send0[s * R + d] + j0) & 0x7FFFFFFFull);
-                        const unsigned long long w1 = static_cast<unsigned long long>(pt.recv0[s * R + d] + j0) & 0x7FFFFFFFull;
-                        const unsigned long long idx = b0 + i;
+                    }
+                    ranges[lane * ndmax + i] = make_int2(gb, ge);
+                    total += ge - gb;
+                }
+            }
+            if (bad) {
+                set_error(p.dev.err, EP_ERR_INVALID_ARG);
+                total = 0;
+            }
+            // where each chunk's commands start in the group's list
+            int incl = total;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += y;
+            }
+            totals[lane] = incl - total;
+            if (lane == 31) totals[32] = incl;
+            __syncwarp();
+        }
+        // post the group's commands, 32 (whole batches) a round; a batch may
+        // span chunks
+        const int gtot = totals[32];
+        for (int r0 = 0; r0 < gtot && !failed; r0 += rs) {
+            const int nround = min(rs, gtot - r0);
+            const bool mine = lane < nround;
+            // command r0 + lane: chunk j (binary search), destination, message
+            unsigned long long w0 = 0ull, w1 = 0ull;
+            if (mine) {
+                const int f0 = r0 + lane;
+                int lo = 0, hi = 31;   // the last chunk j with totals[j] <= f0
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (totals[mid] <= f0) lo = mid; else hi = mid - 1;
+                }
+                const int j = lo;
+                const int s = (grp * 32 + j) / p.chunks_per_rank;
+                const int2 *rg = ranges + j * ndmax;
+                int f = f0 - totals[j], i = 0;
+                int2 g = rg[0];
+                while (f >= g.y - g.x) {
+                    f -= g.y - g.x;
+                    g = rg[++i];
+                }
+                const int d = c + i * C, m = g.x + f;
+                const int j0 = m * G;
+                const int rows = min(G, pt.cnt[s * R + d] - j0);
+                w0 = (static_cast<unsigned long long>(d) << 42) | (static_cast<unsigned long long>(rows) << 31) |
+                     static_cast<unsigned long long>(pt.send0[s * R + d] + j0);
+                w1 = static_cast<unsigned long long>(pt.recv0[s * R + d] + j0);
+            }
+            // batch leaders reserve; every lane learns its batch's base
+            const int n = mine ? min(p.batch, nround - leader) : 0;
+            unsigned long long base = 0ull;
+            if (mine && lane == leader) base = atomicAdd(head, static_cast<unsigned long long>(n));
+            base = __shfl_sync(kFull, base, leader);
+            const unsigned long long idx = base + static_cast<unsigned long long>(lane - leader);
+            bool pending = mine;
+            uint64_t t0 = globaltimer_ns();
+            unsigned sleep = 32;
+            unsigned long long stalls = 0;
+            while (true) {
+                if (pending) {
+                    const unsigned long long tail = ld_acquire_cta_shared(&words[kWProgress]);
+                    if (base + n - tail <= limit) {
                         const unsigned long long lt = lap_tag(idx, p.lg_depth);
                         st_shared_v2(ring + 2 * (idx & dmask), w0 | lt, w1 | lt);
-                        ++cg;
+                        if (lane == leader) {
+                            st.batches += 1;
+                            st.max_batch = max(st.max_batch, static_cast<unsigned>(n));
+                            st.max_inflight = max(st.max_inflight, static_cast<unsigned>(base + n - tail));
+                            st.stalls += stalls;
+                        }
+                        pending = false;
+                    } else {
+                        ++stalls;
                     }
-                    st.batches += 1;
-                    st.max_batch = max(st.max_batch, static_cast<unsigned>(n));
-                    st.max_inflight = max(st.max_inflight, static_cast<unsigned>(b0 + n - retired));
-                    ++q;
-                    progress = true;
                 }
-                if (q == nres) phase = next_res * p.batch < total ? 1 : 3;
-            }
-            if (!__any_sync(kFull, phase < 3)) break;
-            if (__any_sync(kFull, progress)) {
-                if (progress) {
-                    t0 = globaltimer_ns();
-                    sleep = 32;
+                if (!__any_sync(kFull, pending)) break;
+                // waiting touches shared memory only; the device error word
+                // (an L2 round trip) is read every few tens of microseconds
+                bool give_up = false;
+                if (pending) {
+                    const uint64_t now = globaltimer_ns();
+                    if (now - t0 > p.timeout_ns) {
+                        set_error(p.dev.err, EP_ERR_TIMEOUT);
+                        give_up = true;
+                    } else if (now - err_checked > kErrCheckNs) {
+                        err_checked = now;
+                        give_up = read_error(p.dev.err) != 0;
+                    }
                 }
-                continue;
-            }
-            bool give_up = false;
-            if (phase < 3) {
-                if (read_error(p.dev.err) != 0) {
-                    give_up = true;
-                } else if (globaltimer_ns() - t0 > p.timeout_ns) {
-                    set_error(p.dev.err, EP_ERR_TIMEOUT);
-                    give_up = true;
+                if (__any_sync(kFull, give_up)) {
+                    failed = true;
+                    break;
                 }
+                __nanosleep(sleep);
+                sleep = min(sleep * 2u, 64u);
             }
-            if (__any_sync(kFull, give_up)) {
-                failed = true;
-                break;
-            }
-            // lanes waiting on a chunk poll device memory: back off to a few
-            // microseconds (a chunk takes tens); lanes waiting on the ring
-            // poll shared memory: stay quick
-            const unsigned cap = __any_sync(kFull, phase == 2) ? 128u : 4096u;
-            __nanosleep(sleep);
-            sleep = min(sleep * 2u, cap);
         }
+        __syncwarp();
     }
     // statistics: one reduction per warp
     unsigned long long b = st.batches, sp = st.stalls;
@@ -593,7 +680,7 @@ __device__ void consumer_poll(const DispatchParams &p, long long expected, unsig
     window = min(window, 32 * kMaxPollRounds);
     const unsigned long long dmask = static_cast<unsigned long long>(p.D - 1);
     unsigned long long pos = base;
-    uint64_t idle_since = globaltimer_ns();
+    uint64_t idle_since = globaltimer_ns(), err_checked = idle_since;
     unsigned sleep = 32;
     while (pos < end) {
         const int avail = static_cast<int>(min(end - pos, static_cast<unsigned long long>(window)));
@@ -635,10 +722,14 @@ __device__ void consumer_poll(const DispatchParams &p, long long expected, unsig
             idle_since = globaltimer_ns();
             sleep = 32;
         } else {
-            if (read_error(p.dev.err) != 0) break;
-            if (globaltimer_ns() - idle_since > p.timeout_ns) {
+            const uint64_t now = globaltimer_ns();
+            if (now - idle_since > p.timeout_ns) {
                 set_error(p.dev.err, EP_ERR_TIMEOUT);
                 break;
+            }
+            if (now - err_checked > kErrCheckNs) {   // see the posters: an L2 round trip
+                err_checked = now;
+                if (read_error(p.dev.err) != 0) break;
             }
             __nanosleep(sleep);
             sleep = min(sleep * 2u, 128u);
@@ -705,10 +796,11 @@ __device__ void consumer_log(const DispatchParams &p, int c, long long expected,
 
 __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    const SmemLayout L(p.R, p.D, p.stage_bytes, p.stages);
+    const SmemLayout L(p.R, p.C, p.D, p.stage_bytes, p.stages);
     int *rbase = reinterpret_cast<int *>(smem + L.scratch_off);
     unsigned long long *words =
         reinterpret_cast<unsigned long long *>(smem + L.scratch_off + ((p.R + 3) & ~3) * 4);
+    int *ids = reinterpret_cast<int *>(words + kNumWords);
     uint64_t *b = reinterpret_cast<uint64_t *>(smem + L.bar_off);
     Bars bars;
     bars.stage_full = b;
@@ -716,7 +808,6 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
     bars.meta_free = bars.meta_full + kMetaSlots;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool channel_cta = static_cast<int>(blockIdx.x) < p.C;
-    const int qcta = static_cast<int>(blockIdx.x) - p.C, NQ = static_cast<int>(gridDim.x) - p.C;
 
     // Prologue: barriers, window starts, and the checks every CTA takes alike
     // so that either all of them run or none does.
@@ -729,8 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
             }
             mbar_fence_init();
         }
-        words[kWProgress] = 0ull;
-        words[kWStopped] = 0ull;
+        for (int i = 0; i < kNumWords; ++i) words[i] = 0ull;
         words[kWGen] = ld_relaxed_u32(p.dev.disp_gen);
         if (channel_cta) {
             // the ring is drained between calls, so tail is where this call starts
@@ -787,38 +877,42 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
     if (words[kWAbort] == 0ull) {
         if (channel_cta) {
             const int c = blockIdx.x;
-            if (warp < kPosterWarps) {
+            if (warp != kPollWarp && warp != kLogWarp) {
                 PairTables pt;
                 pt.cnt = reinterpret_cast<const int *>(smem);
                 pt.recv0 = pt.cnt + p.R * p.R;
                 pt.send0 = pt.recv0 + p.R * p.R;
-                poster_warp(p, c, warp, words, pt,
-                            reinterpret_cast<unsigned long long *>(smem + SmemLayout::ring_off(p.R)));
+                const int pw = poster_index(warp);
+                uint8_t *rb = smem + SmemLayout::ranges_off(p.R, p.D) + pw * SmemLayout::ranges_bytes_per_warp(p.R, p.C);
+                poster_warp(p, c, pw, words, pt, reinterpret_cast<unsigned long long *>(smem + SmemLayout::ring_off(p.R)),
+                            reinterpret_cast<int2 *>(rb),
+                            reinterpret_cast<int *>(rb + 32 * ((p.R + p.C - 1) / p.C) * 8));
             } else if (!(p.debug & EP_DEBUG_DISABLE_CONSUMER)) {
                 unsigned long long *ring = reinterpret_cast<unsigned long long *>(smem + SmemLayout::ring_off(p.R));
                 unsigned long long *stage = ring + 2 * p.D;
-                if (warp == kPosterWarps)
+                if (warp == kPollWarp)
                     consumer_poll(p, expected, words, ring, stage);
                 else
                     consumer_log(p, c, expected, words, stage);
             }
         } else {
             if (warp == 0)
-                copy_warp(p, smem, L, bars, qcta, NQ, words);
+                copy_warp(p, smem, L, bars, words, ids);
             else if (warp == 1)
-                meta_warp(p, smem, L, bars, rbase, qcta, NQ);
+                meta_warp(p, smem, L, bars, rbase, words, ids);
             else if (warp == 2)
-                notify_warp(p, qcta, NQ, words);
+                notify_warp(p, words, ids);
         }
     }
 
     // Epilogue: the last CTA out advances the dispatch generation (which tags
-    // the chunks' ready flags) and re-arms the counter for the next call.
+    // the chunks' ready flags) and re-arms the counters for the next call.
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
         if (atomicAdd(p.dev.disp_done, 1u) == gridDim.x - 1) {
             *p.dev.disp_done = 0u;
+            *p.dev.chunk_next = 0u;
             atomicAdd(p.dev.disp_gen, 1u);
         }
     }
@@ -849,14 +943,14 @@ ep_status plan_dispatch(ep_ctx *h) {
     const int reserve = 1024;   // static + alignment slack
     int stages = 0;
     for (int s = 15; s >= 3; --s) {
-        SmemLayout L(R, h->cfg.ring_depth, stage_bytes, s);
+        SmemLayout L(R, C, h->cfg.ring_depth, stage_bytes, s);
         if (L.total + reserve <= max_smem) {
             stages = s;
             break;
         }
     }
     if (stages == 0) return EP_ERR_INVALID_ARG;
-    SmemLayout L(R, h->cfg.ring_depth, stage_bytes, stages);
+    SmemLayout L(R, C, h->cfg.ring_depth, stage_bytes, stages);
     h->rows_per_item = rows_per_item;
     h->pieces = pieces;
     h->piece_bytes = piece_bytes;

@@ -50,6 +50,7 @@ struct DevState {
     unsigned int *ready;                // [nchunks] = dispatch generation + 1 once the chunk's rows landed
     unsigned int *disp_gen;             // dispatch calls so far (tags `ready`)
     unsigned int *disp_done;            // CTAs finished in the current dispatch
+    unsigned int *chunk_next;           // next chunk to hand to a copy CTA in the current dispatch
 };
 
 // Layout kernel parameters.
