@@ -86,6 +86,8 @@ _sigs = {
     "ep_ring_stats_get": ([_h, ctypes.POINTER(ep_ring_stats), ctypes.c_int32], ctypes.c_int),
     "ep_check_completion": ([_h, ctypes.c_int32, ctypes.c_uint64], ctypes.c_int),
     "ep_get_info": ([_h, ctypes.POINTER(ep_info)], ctypes.c_int),
+    "ep_layout_static": ([ctypes.POINTER(ep_config), _p, ctypes.POINTER(ep_layout_out),
+                          ctypes.POINTER(ctypes.c_int64), _p], ctypes.c_int),
 }
 for _name, (_args, _res) in _sigs.items():
     _f = getattr(lib, _name)
@@ -174,6 +176,14 @@ def ep_ring_stats_get(h, n: int) -> list:
 
 def ep_check_completion(h, channel: int, cmd_idx: int) -> int:
     return lib.ep_check_completion(h, channel, cmd_idx)
+
+
+def ep_layout_static(cfg: ep_config, topk_idx_ptr: int, out: ep_layout_out, stream: int, want_n: bool = True):
+    """The allocation-free layout (no handle; fixed scratch in the library)."""
+    n = ctypes.c_int64(-1)
+    check(lib.ep_layout_static(ctypes.byref(cfg), topk_idx_ptr, ctypes.byref(out),
+                               ctypes.byref(n) if want_n else None, stream), "ep_layout_static")
+    return int(n.value) if want_n else None
 
 
 def ep_get_info(h) -> dict:

@@ -311,3 +311,107 @@ ep_status launch_layout(ep_ctx *h, const int32_t *topk_idx, const ep_layout_out 
 }
 
 }  // namespace ep
+
+// ---------------------------------------------------------------------------
+// ep_layout_static: the layout above, for callers that cannot allocate device
+// memory.  Its scratch (the look-back descriptors, the histogram, the column
+// prefixes, the counters and the error word) is one file-scope device array
+// of fixed size instead of a handle's cudaMalloc.  Every call on a device
+// shares that array.
+#include <mutex>
+
+namespace ep {
+namespace {
+
+constexpr int kStaticMaxTokens = 262144;   // T = num_ranks * tokens_per_rank
+constexpr int kStaticMaxRanks = 64;
+constexpr int kStaticMaxExperts = 1024;
+constexpr int kStaticMaxTiles = kStaticMaxTokens / 256;
+// byte offsets inside the array (each 256-byte aligned)
+constexpr size_t kSErr = 0, kSTicket = 256, kSDone = 512, kSNRecv = 768, kSPrefix = 1024;
+constexpr size_t kSHist = kSPrefix + ((static_cast<size_t>(kStaticMaxRanks + 1) * kStaticMaxRanks * 4 + 255) / 256) * 256;
+constexpr size_t kSDesc = kSHist + static_cast<size_t>(kStaticMaxRanks) * kStaticMaxExperts * 4;
+constexpr size_t kSBytes = kSDesc + static_cast<size_t>(kStaticMaxTiles) * kStaticMaxRanks * 8;   // about 785 KB
+
+static __device__ __align__(256) unsigned char g_layout_scratch[kSBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void *g_static_addr[kMaxDevices] = {};
+
+// Device address of g_layout_scratch on the current device, looked up once
+// per device.  In host code the array's name is only a stand-in, never a
+// device address.
+ep_status static_scratch(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return EP_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_addr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_layout_scratch) != cudaSuccess || !ptr) return EP_ERR_CUDA;
+        g_static_addr[dev] = ptr;
+    }
+    *out = g_static_addr[dev];
+    return EP_OK;
+}
+
+}  // namespace
+}  // namespace ep
+
+extern "C" ep_status ep_layout_static(const ep_config *cfg, const int32_t *topk_idx, const ep_layout_out *out,
+                                      int64_t *n_recv_host, void *stream) {
+    using namespace ep;
+    if (!cfg || !topk_idx || !out || !out->num_tokens_per_expert || !out->num_tokens_per_rank ||
+        !out->is_token_in_rank || !out->token_slot || !out->recv_off || !out->send_off || !out->msg_count ||
+        !out->recv_count || !out->recv_base || !out->expert_off)
+        return EP_ERR_INVALID_ARG;
+    const ep_status chk = ep_config_check(cfg);
+    if (chk != EP_OK) return chk;
+    const int64_t T = static_cast<int64_t>(cfg->num_ranks) * cfg->tokens_per_rank;
+    if (T > kStaticMaxTokens || cfg->num_ranks > kStaticMaxRanks || cfg->num_experts > kStaticMaxExperts)
+        return EP_ERR_CAPACITY;   // beyond what the fixed scratch holds
+    void *base = nullptr;
+    const ep_status st0 = static_scratch(&base);
+    if (st0 != EP_OK) return st0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned char *b = static_cast<unsigned char *>(base);
+    LayoutParams p{};
+    p.topk_idx = topk_idx;
+    p.out = *out;
+    p.R = cfg->num_ranks;
+    p.Tpr = cfg->tokens_per_rank;
+    p.T = T;
+    p.E = cfg->num_experts;
+    p.K = cfg->topk;
+    p.Er = p.E / p.R;
+    p.G = cfg->rows_per_msg ? cfg->rows_per_msg : (2 * cfg->hidden < 7 * 1024 ? 8 : 1);
+    p.tiles = static_cast<int>((T + 255) / 256);
+    p.dev.err = reinterpret_cast<int32_t *>(b + kSErr);
+    p.dev.ticket = reinterpret_cast<unsigned long long *>(b + kSTicket);
+    p.dev.done = reinterpret_cast<unsigned int *>(b + kSDone);
+    p.dev.n_recv = reinterpret_cast<int64_t *>(b + kSNRecv);
+    p.dev.col_prefix = reinterpret_cast<int32_t *>(b + kSPrefix);
+    p.dev.hist = reinterpret_cast<int32_t *>(b + kSHist);
+    p.dev.tile_desc = reinterpret_cast<unsigned long long *>(b + kSDesc);
+    const uintptr_t a = reinterpret_cast<uintptr_t>(out->is_token_in_rank);
+    p.in_rank_vec = (p.R % 16 == 0 && a % 16 == 0) ? 16 : (p.R % 4 == 0 && a % 4 == 0) ? 4 : 1;
+    // The array keeps the last call's contents: clear what this call needs at
+    // zero (counters, error word, histogram, look-back descriptors).
+    if (cudaMemsetAsync(b, 0, kSPrefix, st) != cudaSuccess ||
+        cudaMemsetAsync(b + kSHist, 0, static_cast<size_t>(p.R) * p.E * 4, st) != cudaSuccess ||
+        cudaMemsetAsync(b + kSDesc, 0, static_cast<size_t>(p.tiles) * p.R * 8, st) != cudaSuccess)
+        return EP_ERR_CUDA;
+    layout_kernel<<<p.tiles, kTile, 0, st>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return EP_ERR_CUDA;
+    if (!n_recv_host) return EP_OK;
+    int64_t n = 0;
+    int32_t code = 0;
+    if (cudaMemcpyAsync(&n, p.dev.n_recv, sizeof(n), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemcpyAsync(&code, p.dev.err, sizeof(code), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return EP_ERR_CUDA;
+    if (code != 0) return static_cast<ep_status>(code);
+    *n_recv_host = n;
+    return EP_OK;
+}
+

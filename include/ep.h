@@ -243,6 +243,35 @@ ep_status ep_check_completion(ep_handle h, int32_t channel, uint64_t cmd_idx);
 /* Launch parameters and allocation size of a handle.  Host only. */
 ep_status ep_get_info(ep_handle h, ep_info *out);
 
+/* ep_layout_static -- ep_layout for callers that cannot allocate device
+ * memory.  The articles have no counterpart: this is a service of this
+ * library.  Some callers cannot call cudaMalloc, and so cannot create a
+ * handle: cudaMalloc may synchronise the whole device, which a serving loop
+ * that must never stall cannot afford, and a framework whose caching
+ * allocator owns all device memory may forbid allocations made behind its
+ * back.  This call allocates nothing (no cudaMalloc, no cudaFree, no
+ * allocating library routine) and needs no handle: the layout's scratch lives
+ * in one fixed device array built into the library, about 785 KB, which every
+ * GPU that loads the library holds until the process exits.
+ *  cfg:         the layer's shape (ep_config_check rules); only num_ranks,
+ *               tokens_per_rank, hidden, num_experts, topk and rows_per_msg
+ *               matter here.  Sizes beyond the array's capacity -- more than
+ *               262144 tokens (num_ranks * tokens_per_rank), 64 ranks or 1024
+ *               experts -- return EP_ERR_CAPACITY and launch nothing.
+ *  topk_idx, out: as for ep_layout (caller-owned device memory); the outputs
+ *               are the ones ep_layout writes.
+ *  n_recv_host: if non-NULL, the call synchronises `stream`, writes N and
+ *               returns the device-side status of this call (EP_ERR_INVALID_ARG
+ *               for a pick outside [-1, E)); if NULL it returns without waiting
+ *               and device-side errors are not reported.
+ * The first call on a device looks up the array's device address (once per
+ * device, under a lock); make that first call before any stream capture.
+ * Every call on a device shares the one array and the call clears the parts
+ * it needs at zero first, so calls must not overlap on the GPU: two calls in
+ * flight at once (on different streams, or from different threads) race. */
+ep_status ep_layout_static(const ep_config *cfg, const int32_t *topk_idx, const ep_layout_out *out,
+                           int64_t *n_recv_host, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
