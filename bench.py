@@ -60,15 +60,27 @@ def read_peaks():
         return 6800.0, "fallback"
 
 
+def kernel_src_sha(kernel: str):
+    """First 16 hex digits of sha256 over the kernel's source file followed by
+    the shared device header: a counter taken on other source does not apply."""
+    import hashlib
+    csrc = os.path.join(ROOT, "combine_ep_layout_04_gb300", "csrc")
+    files = [os.path.join(csrc, f"ep_{kernel}.cu"), os.path.join(csrc, "ep_internal.cuh")]
+    if not all(os.path.exists(f) for f in files):
+        return None
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
 def read_traffic(kernel: str, workload: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
     was taken on the current source of that kernel (else None)."""
-    import hashlib
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    src = os.path.join(ROOT, "combine_ep_layout_04_gb300", "csrc", f"ep_{kernel}.cu")
-    if not os.path.exists(path) or not os.path.exists(src):
+    sha = kernel_src_sha(kernel)
+    if not os.path.exists(path) or sha is None:
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     for line in open(path):
         if line.startswith("#") or "=" not in line:
             continue
@@ -160,7 +172,7 @@ def cpu_oracle_rates(w, idx, wt, x_dev, eo_dev, budget_s: float = 12.0):
         done_tok = t1
     rates["dispatch"] = bytes_disp / t_disp / 1e9
     # combine: a token sample, reading only the rows it needs
-    ntok = 256
+    ntok = max(16, min(256, int(256 * budget_s / 12.0))) if budget_s < 12.0 else 256
     rng = np.random.default_rng(0)
     toks = np.sort(rng.choice(T, min(T, ntok), replace=False))
     need = sorted({int(lay["recv_base"][d]) + int(lay["token_slot"][t, d])
@@ -192,7 +204,7 @@ def step_rate(full: dict, rates: dict) -> tuple[float, float]:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="ht", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -396,8 +408,11 @@ def run_reference(args, w, world, rank):
     # expert output: only the sampled rows are read; draw it lazily by rows
     eo = _LazyRows(eo_rows, w.hidden, w.seed)
     vals = []
+    # each step a bounded sample, sized so that the whole run stays within a
+    # couple of minutes whatever --steps is
+    budget = max(0.1, min(1.0, 90.0 / (args.warmup + args.steps)))
     for i in range(args.warmup + args.steps):
-        rates, full, note = cpu_oracle_rates(w, idx, wt, x, eo, budget_s=1.0)
+        rates, full, note = cpu_oracle_rates(w, idx, wt, x, eo, budget_s=budget)
         v, secs = step_rate(full, rates)
         if i >= args.warmup:
             vals.append((v, secs))

@@ -17,8 +17,9 @@
 //
 // How: one persistent cooperative kernel, one CTA per SM, in two kinds.
 //
-// Copy CTAs (all but the first C) move the rows.  Chunks of 32 tokens of one
-// source rank are drawn from a device-wide counter (so faster SMs take more);
+// Copy CTAs (all but the first C) move the rows.  Chunks of 8 to 32 tokens of
+// one source rank (about four per copy CTA at most) are drawn from a
+// device-wide counter (so faster SMs take more);
 // three warps hand each chunk on through mbarriers and shared counters:
 //   copy    1-D TMA bulk loads of token rows (a run of whole rows when they
 //           are small, a piece of one row when it is large) into a ring of
@@ -124,11 +125,11 @@ struct MetaSlot {
 
 __device__ __forceinline__ int chunk_ntok(const DispatchParams &p, int k) {
     const int ci = k % p.chunks_per_rank;
-    return min(kChunkTokens, p.Tpr - ci * kChunkTokens);
+    return min(p.chunk_tokens, p.Tpr - ci * p.chunk_tokens);
 }
 __device__ __forceinline__ int64_t chunk_tok0(const DispatchParams &p, int k) {
     const int s = k / p.chunks_per_rank, ci = k % p.chunks_per_rank;
-    return static_cast<int64_t>(s) * p.Tpr + static_cast<int64_t>(ci) * kChunkTokens;
+    return static_cast<int64_t>(s) * p.Tpr + static_cast<int64_t>(ci) * p.chunk_tokens;
 }
 __device__ __forceinline__ int chunk_items(const DispatchParams &p, int ntok) {
     return p.pieces > 1 ? ntok * p.pieces : (ntok + p.rows_per_item - 1) / p.rows_per_item;
@@ -927,10 +928,17 @@ ep_status plan_dispatch(ep_ctx *h) {
     const int R = h->cfg.num_ranks, C = h->cfg.channels;
     const int64_t B = 2ll * h->cfg.hidden;
     const int kTargetStage = 16384;
+    // Chunk size: about four chunks per copy CTA, so that the dynamic draw
+    // balances the load even when the batch is small, 8 to 32 tokens (the
+    // meta warp takes one token per lane).
+    const int64_t T = static_cast<int64_t>(R) * h->cfg.tokens_per_rank;
+    const int64_t copy_ctas = h->sm_count > C ? h->sm_count - C : 1;
+    int chunk_tokens = kChunkTokens;
+    while (chunk_tokens > 8 && T < 4 * copy_ctas * chunk_tokens) chunk_tokens /= 2;
     int rows_per_item = 1, pieces = 1, piece_bytes = static_cast<int>(B);
     if (B <= kTargetStage) {
         rows_per_item = static_cast<int>(kTargetStage / B);
-        if (rows_per_item > kChunkTokens) rows_per_item = kChunkTokens;
+        if (rows_per_item > chunk_tokens) rows_per_item = chunk_tokens;
         piece_bytes = static_cast<int>(B);
     } else {
         pieces = static_cast<int>((B + kTargetStage - 1) / kTargetStage);
@@ -961,7 +969,8 @@ ep_status plan_dispatch(ep_ctx *h) {
     h->meta_slots = kMetaSlots;
     h->disp_smem = static_cast<size_t>(L.total);
     h->disp_threads = kThreads;
-    h->chunks_per_rank = (h->cfg.tokens_per_rank + kChunkTokens - 1) / kChunkTokens;
+    h->chunk_tokens = chunk_tokens;
+    h->chunks_per_rank = (h->cfg.tokens_per_rank + chunk_tokens - 1) / chunk_tokens;
     h->nchunks = h->chunks_per_rank * R;
     if (cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(h->disp_smem)) != cudaSuccess)
@@ -1004,6 +1013,7 @@ ep_status launch_dispatch(ep_ctx *h, const void *x, const ep_layout_out *lay, vo
     p.drain_batch = h->cfg.drain_batch;
     p.debug = h->cfg.debug_flags;
     p.chunks_per_rank = h->chunks_per_rank;
+    p.chunk_tokens = h->chunk_tokens;
     p.nchunks = h->nchunks;
     p.rows_per_item = h->rows_per_item;
     p.pieces = h->pieces;

@@ -15,7 +15,7 @@ namespace ep {
 constexpr int kMaxRanks = 64;
 constexpr int kMaxTopk = 32;
 constexpr int kMaxChannels = 64;
-constexpr int kChunkTokens = 32;         // dispatch: tokens per chunk (one per lane)
+constexpr int kChunkTokens = 32;         // dispatch: most tokens per chunk (one per lane)
 constexpr int kHeadStride = 16;          // u64s between two channels' head/tail words (128 B)
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
@@ -77,6 +77,7 @@ struct DispatchParams {
     uint64_t timeout_ns;
     int R, Tpr, C, D, max_inflight, batch, G, drain_batch, debug;
     int chunks_per_rank, nchunks;
+    int chunk_tokens;    // tokens per chunk (8..32)
     int rows_per_item;   // tokens per item when a row fits a stage, else 1
     int pieces;          // pieces per row when it does not, else 1
     int piece_bytes;     // bytes per piece (a multiple of 16)
@@ -118,7 +119,7 @@ struct ep_ctx {
     size_t disp_smem;
     int stage_bytes, stages, prefetch, meta_slots, store_lag;
     int rows_per_item, pieces, piece_bytes;
-    int chunks_per_rank, nchunks;
+    int chunks_per_rank, nchunks, chunk_tokens;
     int64_t log_cap;
     // combine geometry
     int comb_grid, comb_threads;

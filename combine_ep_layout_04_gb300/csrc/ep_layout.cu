@@ -41,34 +41,45 @@ __device__ __forceinline__ unsigned long long pack_desc(uint32_t epoch, uint32_t
     return (static_cast<unsigned long long>(epoch) << 34) | (static_cast<unsigned long long>(flag) << 32) | value;
 }
 
-// Exclusive scan of s[0, n) in place by the whole block (blockDim == kTile).
-// Returns the total.  `tmp` holds kTile + 1 ints.
+// Exclusive scan of s[0, n) in place by the whole block (blockDim == kTile):
+// each thread scans a run of consecutive items, warps scan the run totals with
+// shuffles, one warp scans the warp totals.  Returns the total.  `tmp` holds
+// at least kWarps + 1 ints.
 __device__ int block_excl_scan(int *s, int n, int *tmp) {
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int per = (n + kTile - 1) / kTile;
     const int b = tid * per, e = min(n, b + per);
     int local = 0;
     for (int i = b; i < e; ++i) local += s[i];
-    tmp[tid] = local;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) tmp[warp] = incl;
     __syncthreads();
-    if (tid == 0) {
-        int run = 0;
-        for (int i = 0; i < kTile; ++i) {
-            int v = tmp[i];
-            tmp[i] = run;
-            run += v;
+    if (warp == 0) {
+        const int v = lane < kWarps ? tmp[lane] : 0;
+        int wi = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFull, wi, o);
+            if (lane >= o) wi += y;
         }
-        tmp[kTile] = run;
+        if (lane < kWarps) tmp[lane] = wi - v;
+        if (lane == kWarps - 1) tmp[kWarps] = wi;
     }
     __syncthreads();
-    int run = tmp[tid];
+    int run = tmp[warp] + incl - local;
     for (int i = b; i < e; ++i) {
-        int v = s[i];
+        const int v = s[i];
         s[i] = run;
         run += v;
     }
+    const int total = tmp[kWarps];
     __syncthreads();
-    return tmp[kTile];
+    return total;
 }
 
 // The last tile to finish: counts and small scans from the column prefixes
@@ -90,25 +101,38 @@ __device__ void finish_layout(const LayoutParams &p, int *s_work, int *s_tmp) {
     __syncthreads();
     block_excl_scan(s_work, R * R, s_tmp);   // row-major send order
     for (int i = tid; i < R * R; i += kTile) p.out.send_off[i] = s_work[i];
-    __syncthreads();
-    if (tid == 0) {
+    // window sizes and starts (one warp)
+    if (tid < 32) {
         int64_t run = 0;
-        for (int d = 0; d < R; ++d) {
-            const int c = __ldcg(P + R * R + d);
-            p.out.recv_count[d] = c;
-            p.out.recv_base[d] = static_cast<int32_t>(run);
-            run += c;
+        for (int d0 = 0; d0 < R; d0 += 32) {
+            const int d = d0 + tid;
+            const int c = d < R ? __ldcg(P + R * R + d) : 0;
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFull, incl, o);
+                if (tid >= o) incl += y;
+            }
+            if (d < R) {
+                p.out.recv_count[d] = c;
+                p.out.recv_base[d] = static_cast<int32_t>(run + incl - c);
+            }
+            run += __shfl_sync(kFull, incl, 31);
         }
-        *p.dev.n_recv = run;
+        if (tid == 0) *p.dev.n_recv = run;
     }
-    // expert totals: copy the histogram out, clear the scratch
-    for (int e = tid; e < E; e += kTile) s_work[e] = 0;
     __syncthreads();
-    for (int i = tid; i < R * E; i += kTile) {
-        const int v = __ldcg(p.dev.hist + i);
-        p.out.num_tokens_per_expert[i] = v;
-        p.dev.hist[i] = 0;
-        atomicAdd(&s_work[i % E], v);
+    // expert totals: each thread sums one expert over the source ranks,
+    // copying the histogram out and clearing the scratch as it goes
+    for (int e = tid; e < E; e += kTile) {
+        int tot = 0;
+        for (int s = 0; s < R; ++s) {
+            const int v = __ldcg(p.dev.hist + static_cast<int64_t>(s) * E + e);
+            p.out.num_tokens_per_expert[static_cast<int64_t>(s) * E + e] = v;
+            p.dev.hist[static_cast<int64_t>(s) * E + e] = 0;
+            tot += v;
+        }
+        s_work[e] = tot;
     }
     __syncthreads();
     block_excl_scan(s_work, E, s_tmp);
