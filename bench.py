@@ -210,6 +210,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens-per-rank", type=int, default=0,
+                    help="override the workload's tokens per rank (smaller cases for profiler captures)")
+    ap.add_argument("--sweep", choices=["msg"], default=None,
+                    help="msg: dispatch bandwidth against row and message size, one JSON line per point")
     args = ap.parse_args()
     assert args.warmup >= 3 or os.environ.get("EP_BENCH_ALLOW_SHORT_WARMUP"), "warm-up must be >= 3 steps"
 
@@ -221,7 +225,11 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     w = W.get(args.workload)
+    if args.tokens_per_rank:
+        w = w.replace(tokens_per_rank=args.tokens_per_rank, name=f"{w.name}-tpr{args.tokens_per_rank}")
 
+    if args.sweep:
+        return run_sweep(args)
     if args.impl == "reference":
         return run_reference(args, w, world, rank)
 
@@ -312,7 +320,7 @@ def main():
     achieved = ab[dom] / per_op[dom] / 1e9
     roofline = {"kernel": f"{dom}_kernel", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                 "peak_kind": f"{peak_kind} hbm_gbs (copy)", "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "traffic": read_traffic(dom, args.workload),
+                "traffic": read_traffic(dom, w.name),
                 "algorithmic_bytes_per_launch": ab[dom],
                 "per_op": {k: {"us": round(per_op[k] * 1e6, 2), "bytes": ab[k],
                                "GBps": round(ab[k] / per_op[k] / 1e9, 1),
@@ -322,7 +330,8 @@ def main():
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K_,
         "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "num_tokens": T,
+        "config": {"workload": WORKLOAD_TEXT[args.workload] + (
+                       f" (tokens per rank {Tpr})" if args.tokens_per_rank else ""), "name": w.name, "num_tokens": T,
                    "hidden": H, "ranks": R, "experts": E, "topk": K, "n_recv": N, "messages": n_msgs,
                    "rows_per_msg": layer.G, "l2": "flushed between steps (write of 2x L2, outside the events)",
                    "parallelism": "replicas" if world > 1 else "1 GPU"},
@@ -348,47 +357,156 @@ def main():
     if dist:
         dist.destroy_process_group()
 
+# --------------------------------------------------------------------- sweep
+SWEEP_ROW_BYTES = (1024, 2048, 4096, 7168, 8192, 14336, 28672, 57344)
+SWEEP_MSG_ROWS = (1, 4, 16, 64, 256, 1024)
+
+
+def sweep_points():
+    """(row bytes B, rows per message G) pairs: every row size at G = 1, the
+    packing threshold (4 KB and 7 KB rows at G = 1 and 8), and message sizes
+    from 1 KB to 16 MB at B = 1 KB and B = 16 KB."""
+    pts = [(b, 1) for b in SWEEP_ROW_BYTES]
+    pts += [(b, 8) for b in (4096, 7168)]
+    pts += [(b, g) for b in (1024, 16384) for g in SWEEP_MSG_ROWS if g > 1]
+    return pts
+
+
+def run_sweep(args):
+    """Dispatch (with its TransferCmd rings) on DeepSeek-V3-shaped routing (32
+    ranks, 256 experts, top-8 uniform) at each (B, G): tokens per rank are
+    chosen so that the received payload is about 4 GB and every (source,
+    destination) pair holds at least G rows on average.  Median of 20
+    launches, L2 flushed before each.  A one-token, one-message dispatch of a
+    16-byte row gives the small-message latency (launch included)."""
+    import torch
+
+    import workloads as W
+    from combine_ep_layout_04_gb300 import EpLayer
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    peak, peak_kind = read_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    flush = torch.empty(2 * (getattr(props, "L2_cache_size", 0) or 128 * 2**20), dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream(dev)
+    R, E, K = 32, 256, 8
+    cases = [("latency", W.Workload("sweep-latency", 1, 1, 8, 1, 1, seed=606), 1)]
+    for b, g in sweep_points():
+        frac_dst = 1.0 - np.prod([(E - E // R - i) / (E - i) for i in range(K)])
+        tpr = int(4 * 2**30 / (R * R * frac_dst * b))
+        tpr = max(tpr, int(np.ceil(g / frac_dst)))
+        cases.append((f"B{b}_G{g}", W.Workload(f"sweep-B{b}-G{g}", R, tpr, b // 2, E, K, seed=707), g))
+    for label, w, g in cases:
+        idx, _ = W.make_routing(w)
+        topk = torch.from_numpy(idx).to(dev)
+        x = W.make_x_torch(w, dev)
+        with EpLayer(w.num_ranks, w.tokens_per_rank, w.hidden, w.num_experts, w.topk, rows_per_msg=g,
+                     device=dev) as layer:
+            lay = layer.layout(topk)
+            N = lay.n_recv
+            recv = torch.empty((N, w.hidden), dtype=torch.bfloat16, device=dev)
+            n_msgs = int(lay.msg_count.sum())
+            n_sent = int((lay.is_token_in_rank.sum(dim=1) > 0).sum())
+            ab = algorithmic_bytes(w.num_ranks, w.num_tokens, w.hidden, w.num_experts, w.topk, N, n_msgs,
+                                   n_sent)["dispatch"]
+            times = []
+            for i in range(23):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                layer.dispatch(x, lay, recv)
+                e1.record(st)
+                torch.cuda.synchronize(dev)
+                if i >= 3:
+                    times.append(e0.elapsed_time(e1) * 1e-3)
+            if layer.device_status() != 0:
+                raise SystemExit(f"device status {layer.device_status()} at {label}")
+            t = float(np.median(times))
+            row = {"sweep": "msg", "point": label, "row_bytes": 2 * w.hidden, "rows_per_msg": g,
+                   "msg_bytes": 2 * w.hidden * g, "tokens_per_rank": w.tokens_per_rank, "n_recv": N,
+                   "messages": n_msgs, "dispatch_us": round(t * 1e6, 2),
+                   "GBps": round(ab / t / 1e9, 1), "frac": round(ab / t / 1e9 / peak, 4),
+                   "peak": f"{peak} ({peak_kind})", "Mmsgs_per_s": round(n_msgs / t / 1e6, 2)}
+            print(json.dumps(row), flush=True)
+            del recv
+        del x, topk
+
 
 def run_e2e(layer, w, idx, wt, x_dev, lay, recv, out, ab, dev, K_):
-    """The same step through the public API with host buffers: pinned host ->
-    device copies of x, topk_idx and topk_weights, layout, dispatch, identity
-    expert (combine reads the receive buffer), combine, device -> host copy of
-    the output; all inside the timed region."""
+    """The same step through the public API with host buffers.  Every step
+    copies its x, topk_idx and topk_weights from pinned host memory to the
+    device, runs layout, dispatch, the identity expert (combine reads the
+    receive buffer) and combine, and copies its output back to pinned host
+    memory; all inside the timed region.  Steps are pipelined the way a
+    serving loop would run them: the host->device copy of step i+1 and the
+    device->host copy of step i-1 run on their own streams (one copy engine
+    each way) while step i computes; inputs and outputs are double-buffered,
+    and events order every reuse of a buffer."""
     import torch
     T, H, K = w.num_tokens, w.hidden, w.topk
     x_h = x_dev.cpu().pin_memory()
     idx_h = torch.from_numpy(idx).pin_memory()
     wt_h = torch.from_numpy(wt).pin_memory()
-    out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    x_d = torch.empty_like(x_dev)
-    idx_d = torch.empty((T, K), dtype=torch.int32, device=dev)
-    wt_d = torch.empty((T, K), dtype=torch.float32, device=dev)
+    out_h = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    x_d = [torch.empty_like(x_dev) for _ in range(2)]
+    idx_d = [torch.empty((T, K), dtype=torch.int32, device=dev) for _ in range(2)]
+    wt_d = [torch.empty((T, K), dtype=torch.float32, device=dev) for _ in range(2)]
+    out_d = [out, torch.empty_like(out)]
+    comp = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    inputs_free = [ev(), ev()]      # compute no longer reads input buffer b
+    inputs_ready = [ev(), ev()]     # input buffer b holds this step's inputs
+    out_ready = [ev(), ev()]        # output buffer b holds this step's result
+    out_free = [ev(), ev()]         # output buffer b has been copied to the host
+    for b in range(2):
+        inputs_free[b].record(comp)
+        out_free[b].record(comp)
 
-    def step():
-        x_d.copy_(x_h, non_blocking=True)
-        idx_d.copy_(idx_h, non_blocking=True)
-        wt_d.copy_(wt_h, non_blocking=True)
-        layer.layout(idx_d, out=lay, sync=False)
-        layer.dispatch(x_d, lay, recv)
-        layer.combine(recv, wt_d, idx_d, lay, out)
-        out_h.copy_(out, non_blocking=True)
+    def step(i):
+        b = i & 1
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(inputs_free[b])
+            x_d[b].copy_(x_h, non_blocking=True)
+            idx_d[b].copy_(idx_h, non_blocking=True)
+            wt_d[b].copy_(wt_h, non_blocking=True)
+            inputs_ready[b].record(s_in)
+        comp.wait_event(inputs_ready[b])
+        comp.wait_event(out_free[b])
+        layer.layout(idx_d[b], out=lay, sync=False)
+        layer.dispatch(x_d[b], lay, recv)
+        layer.combine(recv, wt_d[b], idx_d[b], lay, out_d[b])
+        inputs_free[b].record(comp)
+        out_ready[b].record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(out_ready[b])
+            out_h[b].copy_(out_d[b], non_blocking=True)
+            out_free[b].record(s_out)
 
-    for _ in range(3):
-        step()
+    for i in range(3):
+        step(i)
     torch.cuda.synchronize(dev)
-    st = torch.cuda.current_stream(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for _ in range(K_):
-        step()
-    e1.record(st)
+    e0.record(comp)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    for i in range(K_):
+        step(i)
+    done = ev()
+    done.record(s_out)
+    comp.wait_event(done)
+    e1.record(comp)
     torch.cuda.synchronize(dev)
     secs = e0.elapsed_time(e1) * 1e-3 / K_
+    if layer.device_status() != 0:
+        raise SystemExit(f"device status {layer.device_status()} in the end-to-end run")
     h2d = x_h.numel() * 2 + idx_h.numel() * 4 + wt_h.numel() * 4
-    d2h = out_h.numel() * 2
+    d2h = out_h[0].numel() * 2
     return {"value": round(sum(ab.values()) / secs / 1e9, 1), "unit": "GB/s", "ms_per_step": round(secs * 1e3, 3),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": K_,
-            "note": "pinned host buffers; identity expert between dispatch and combine"}
+            "note": "pinned host buffers, copies of step i+1 in and i-1 out overlapped with step i; "
+                    "identity expert between dispatch and combine"}
 
 
 def run_reference(args, w, world, rank):
