@@ -77,6 +77,8 @@ def _load():
         lib.oracle_descriptors.restype = None
         lib.oracle_combine.argtypes = [i32, i32, i32, i64, i64, i64, p, p, p, p, p, i64, p]
         lib.oracle_combine.restype = i32
+        lib.oracle_expert_layout.argtypes = [i32, i32, i32, i32, p, p, p, p, p, i64, p, p, p, p, p]
+        lib.oracle_expert_layout.restype = i32
         lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
         lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
         lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
@@ -186,6 +188,36 @@ def combine(lay: dict, topk_idx: np.ndarray, topk_weights: np.ndarray, experts_p
                             _ptr(expert_out_bits), n_rows, _ptr(out))
     if rc != 0:
         raise OracleError(f"oracle_combine: code {rc}")
+    return out
+
+
+def expert_layout(lay: dict, topk_idx: np.ndarray, topk_weights: np.ndarray, num_experts: int) -> dict:
+    """Expert-major receive metadata (UCCL-EP s1 token-level routing to the
+    experts of each pick): per receive row its source token and its local
+    picks and weights; per expert the receive rows of its picks in pick order.
+    Definitions in ep_oracle.c.  Returns recv_topk_idx int32 [N, K],
+    recv_topk_weights float32 [N, K], recv_src_token int32 [N], expert_rows
+    int32 [picks], expert_count int32 [E]."""
+    lib = _load()
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    topk_weights = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    T, K = topk_idx.shape
+    R = lay["recv_base"].shape[0]
+    E = num_experts
+    N = lay["n_recv"]
+    out = {
+        "recv_topk_idx": np.zeros((N, K), np.int32),
+        "recv_topk_weights": np.zeros((N, K), np.float32),
+        "recv_src_token": np.zeros((N,), np.int32),
+        "expert_rows": np.zeros((int((topk_idx >= 0).sum()),), np.int32),
+        "expert_count": np.zeros((E,), np.int32),
+    }
+    rc = lib.oracle_expert_layout(R, T // R, E, K, _ptr(topk_idx), _ptr(topk_weights), _ptr(lay["token_slot"]),
+                                  _ptr(lay["recv_base"]), _ptr(lay["expert_off"]), N,
+                                  *[_ptr(out[k]) for k in ("recv_topk_idx", "recv_topk_weights",
+                                                           "recv_src_token", "expert_rows", "expert_count")])
+    if rc != 0:
+        raise OracleError(f"oracle_expert_layout: code {rc}")
     return out
 
 

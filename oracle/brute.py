@@ -100,6 +100,39 @@ def descriptors(lay: dict, C: int, G: int, B: int) -> list[list[tuple]]:
     return chans
 
 
+def expert_layout(lay: dict, topk_idx, topk_weights, E: int) -> dict:
+    """Expert-major receive metadata by search and sort: each receive row is
+    matched to its (token, rank) by scanning all pairs; each expert's rows
+    come from sorting all picks by (expert, token, k) with Python's sort."""
+    T, R = lay["token_slot"].shape
+    Er = E // R
+    n = lay["n_recv"]
+    picks = [[int(v) for v in row] for row in topk_idx]
+    K = len(picks[0]) if T else 0
+
+    def row_of(t, d):
+        return int(lay["recv_base"][d]) + int(lay["token_slot"][t][d])
+
+    src = np.zeros((n,), np.int32)
+    ridx = np.zeros((n, K), np.int32)
+    rw = np.zeros((n, K), np.float32)
+    for row in range(n):
+        owners = [(t, d) for t in range(T) for d in range(R)
+                  if lay["token_slot"][t][d] >= 0 and row_of(t, d) == row]
+        assert len(owners) == 1, owners
+        t, d = owners[0]
+        src[row] = t
+        for k, e in enumerate(picks[t]):
+            on_d = e != -1 and e // Er == d
+            ridx[row, k] = e - d * Er if on_d else -1
+            rw[row, k] = topk_weights[t][k] if on_d else 0.0
+    triples = sorted((e, t, k) for t in range(T) for k, e in enumerate(picks[t]) if e != -1)
+    rows = [row_of(t, e // Er) for (e, t, k) in triples]
+    count = [sum(1 for (f, _, _) in triples if f == e) for e in range(E)]
+    return {"recv_topk_idx": ridx, "recv_topk_weights": rw, "recv_src_token": src,
+            "expert_rows": np.array(rows, np.int32), "expert_count": np.array(count, np.int32)}
+
+
 # ------------------------------------------------------ exact rounding helpers
 
 

@@ -313,3 +313,80 @@ int oracle_combine(int R, int Er, int K, int64_t H, int64_t t_begin, int64_t t_e
     free(acc);
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------------- expert layout -- */
+
+/*
+ * Expert-major receive metadata: what a rank needs after dispatch to run its
+ * local experts on the rows it received ([UCCL-EP] s1: each token goes to the
+ * experts of its top-k picks; the grouped expert step consumes the received
+ * rows per expert).
+ *
+ * For every receive row n = recv_base[d] + token_slot[t][d]:
+ *   recv_src_token[n]       = t
+ *   recv_topk_idx[n][k]     = topk_idx[t][k] - d*Er  if pick k lives on rank d,
+ *                             else -1
+ *   recv_topk_weights[n][k] = topk_weights[t][k]     if pick k lives on rank d,
+ *                             else 0.0f
+ * and, taking the picks (t, k) in increasing t, then k:
+ *   expert_rows[expert_off[e] + j] = receive row of the j-th pick of expert e
+ *                                    (row of (t, rank of e))
+ *   expert_count[e]                = number of picks of expert e
+ * expert_rows therefore lists, per expert, the rows it must process in
+ * increasing receive-row order.  A token naming one expert twice has no
+ * well-defined position and is rejected (ORACLE_BAD_TOPK), as is a pick
+ * outside [-1, E).  recv_* must hold n_recv rows; expert_rows must hold one
+ * entry per pick that is not -1.
+ */
+int oracle_expert_layout(int R, int Tpr, int E, int K, const int32_t *topk_idx,
+                         const float *topk_weights, const int32_t *token_slot,
+                         const int32_t *recv_base, const int32_t *expert_off, int64_t n_recv,
+                         int32_t *recv_topk_idx, float *recv_topk_weights,
+                         int32_t *recv_src_token, int32_t *expert_rows, int32_t *expert_count) {
+    if (R <= 0 || Tpr < 0 || E <= 0 || K <= 0 || E % R != 0) return ORACLE_BAD_ARG;
+    const int64_t T = (int64_t)R * Tpr;
+    const int Er = E / R;
+
+    /* picks must be -1 or an expert, and distinct within a token */
+    for (int64_t t = 0; t < T; ++t)
+        for (int k = 0; k < K; ++k) {
+            int32_t e = topk_idx[t * K + k];
+            if (e == -1) continue;
+            if (e < -1 || e >= E) return ORACLE_BAD_TOPK;
+            for (int k2 = 0; k2 < k; ++k2)
+                if (topk_idx[t * K + k2] == e) return ORACLE_BAD_TOPK;
+        }
+
+    /* 1. per receive row: source token, local picks and their weights */
+    for (int64_t t = 0; t < T; ++t)
+        for (int d = 0; d < R; ++d) {
+            int32_t slot = token_slot[t * R + d];
+            if (slot < 0) continue;
+            int64_t n = (int64_t)recv_base[d] + slot;
+            if (n < 0 || n >= n_recv) return ORACLE_BAD_ARG;
+            recv_src_token[n] = (int32_t)t;
+            for (int k = 0; k < K; ++k) {
+                int32_t e = topk_idx[t * K + k];
+                if (e >= 0 && e / Er == d) {
+                    recv_topk_idx[n * K + k] = e - d * Er;
+                    recv_topk_weights[n * K + k] = topk_weights[t * K + k];
+                } else {
+                    recv_topk_idx[n * K + k] = -1;
+                    recv_topk_weights[n * K + k] = 0.0f;
+                }
+            }
+        }
+
+    /* 2. per expert: its picks' receive rows, in pick order */
+    for (int e = 0; e < E; ++e) expert_count[e] = 0;
+    for (int64_t t = 0; t < T; ++t)
+        for (int k = 0; k < K; ++k) {
+            int32_t e = topk_idx[t * K + k];
+            if (e < 0) continue;
+            int d = e / Er;
+            int64_t row = (int64_t)recv_base[d] + token_slot[t * R + d];
+            expert_rows[(int64_t)expert_off[e] + expert_count[e]] = (int32_t)row;
+            expert_count[e] += 1;
+        }
+    return ORACLE_OK;
+}
