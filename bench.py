@@ -344,6 +344,7 @@ def main():
         "wall_s_timed_region": round(wall1 - wall0, 3),
     }
 
+    result["next_rows"] = {"expert_layout": time_expert_layout(layer, topk, wts, lay, flush, st, peak, w, N)}
     if not args.no_e2e:
         result["e2e"] = run_e2e(layer, w, idx, wt, x, lay, recv, out, ab, dev, K_=max(3, min(K_, 10)))
     if rank == 0 and not args.no_cpu_baseline and world == 1:
@@ -356,6 +357,31 @@ def main():
         print(json.dumps(result))
     if dist:
         dist.destroy_process_group()
+
+def time_expert_layout(layer, topk, wts, lay, flush, st, peak, w, N, reps: int = 20):
+    """ep_expert_layout timed on its own (it is not part of the step): median
+    of `reps` launches with the L2 flushed before each."""
+    import torch
+    lay.n_recv = N            # the step's layouts ran without waiting for N
+    xl = layer.expert_layout(topk, wts, lay)
+    T, K, E = w.num_tokens, w.topk, w.num_experts
+    M = int((topk >= 0).sum())
+    nbytes = T * K * 8 + N * 4 + N * (8 * K + 4) + M * 4 + E * 4
+    times = []
+    for _ in range(reps + 3):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        layer.expert_layout(topk, wts, lay, out=xl)
+        e1.record(st)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e-3)
+    if layer.device_status() != 0:
+        raise SystemExit(f"device status {layer.device_status()} in the expert layout")
+    t = float(np.median(times[3:]))
+    return {"us": round(t * 1e6, 2), "bytes": nbytes, "GBps": round(nbytes / t / 1e9, 1),
+            "frac": round(nbytes / t / 1e9 / peak, 4), "launches": reps}
+
 
 # --------------------------------------------------------------------- sweep
 SWEEP_ROW_BYTES = (1024, 2048, 4096, 7168, 8192, 14336, 28672, 57344)

@@ -42,6 +42,11 @@ class ep_layout_out(ctypes.Structure):
         "send_off", "msg_count", "recv_count", "recv_base", "expert_off")]
 
 
+class ep_expert_layout_out(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "recv_topk_idx", "recv_topk_weights", "recv_src_token", "expert_rows", "expert_count")]
+
+
 class ep_cmd_log(ctypes.Structure):
     _fields_ = [("cmds", ctypes.c_void_p), ("count", ctypes.c_void_p),
                 ("capacity_per_channel", ctypes.c_int64), ("channels", ctypes.c_int32)]
@@ -82,6 +87,8 @@ _sigs = {
     "ep_layout": ([_h, _p, ctypes.POINTER(ep_layout_out), ctypes.POINTER(ctypes.c_int64), _p], ctypes.c_int),
     "ep_dispatch": ([_h, _p, ctypes.POINTER(ep_layout_out), _p, ctypes.c_int64, _p], ctypes.c_int),
     "ep_combine": ([_h, _p, ctypes.c_int64, _p, _p, ctypes.POINTER(ep_layout_out), _p, _p], ctypes.c_int),
+    "ep_expert_layout": ([_h, _p, _p, ctypes.POINTER(ep_layout_out), ctypes.POINTER(ep_expert_layout_out),
+                          ctypes.c_int64, ctypes.c_int64, _p], ctypes.c_int),
     "ep_cmd_log_get": ([_h, ctypes.POINTER(ep_cmd_log)], ctypes.c_int),
     "ep_ring_stats_get": ([_h, ctypes.POINTER(ep_ring_stats), ctypes.c_int32], ctypes.c_int),
     "ep_check_completion": ([_h, ctypes.c_int32, ctypes.c_uint64], ctypes.c_int),
@@ -160,6 +167,12 @@ def ep_combine(h, expert_out_ptr: int, expert_out_rows: int, weights_ptr: int, t
                layout: ep_layout_out, out_ptr: int, stream: int) -> None:
     check(lib.ep_combine(h, expert_out_ptr, expert_out_rows, weights_ptr, topk_idx_ptr, ctypes.byref(layout),
                          out_ptr, stream), "ep_combine")
+
+
+def ep_expert_layout(h, topk_idx_ptr: int, weights_ptr: int, layout: ep_layout_out, out: ep_expert_layout_out,
+                     recv_rows: int, rows_cap: int, stream: int) -> None:
+    check(lib.ep_expert_layout(h, topk_idx_ptr, weights_ptr, ctypes.byref(layout), ctypes.byref(out), recv_rows,
+                               rows_cap, stream), "ep_expert_layout")
 
 
 def ep_cmd_log_get(h) -> ep_cmd_log:

@@ -121,7 +121,8 @@ ep_status ep_create(const ep_config *cfg, ep_handle *out) {
     const int64_t ranks_per_chan = (R + C - 1) / C;
     const int64_t kmin = cfg->topk < ranks_per_chan ? cfg->topk : ranks_per_chan;
     h->log_cap = (T * kmin + h->G - 1) / h->G + static_cast<int64_t>(R) * ranks_per_chan;
-    if ((st = ep::plan_dispatch(h)) != EP_OK || (st = ep::plan_combine(h)) != EP_OK) {
+    if ((st = ep::plan_dispatch(h)) != EP_OK || (st = ep::plan_combine(h)) != EP_OK ||
+        (st = ep::plan_expert_layout(h)) != EP_OK) {
         delete h;
         return st;
     }
@@ -144,6 +145,8 @@ ep_status ep_create(const ep_config *cfg, ep_handle *out) {
     const size_t o_gen = cv.take<unsigned int>(1);
     const size_t o_ddone = cv.take<unsigned int>(1);
     const size_t o_cnext = cv.take<unsigned int>(1);
+    const size_t o_xticket = cv.take<unsigned long long>(1);
+    const size_t o_xdesc = cv.take<unsigned long long>(static_cast<size_t>(h->xtiles) * E);
     h->alloc_bytes = cv.off;
     if (cudaMalloc(&h->alloc_base, h->alloc_bytes) != cudaSuccess) {
         delete h;
@@ -173,6 +176,8 @@ ep_status ep_create(const ep_config *cfg, ep_handle *out) {
     d.disp_gen = reinterpret_cast<unsigned int *>(b + o_gen);
     d.disp_done = reinterpret_cast<unsigned int *>(b + o_ddone);
     d.chunk_next = reinterpret_cast<unsigned int *>(b + o_cnext);
+    d.xticket = reinterpret_cast<unsigned long long *>(b + o_xticket);
+    d.xdesc = reinterpret_cast<unsigned long long *>(b + o_xdesc);
     if (cudaDeviceSynchronize() != cudaSuccess) {
         cudaFree(h->alloc_base);
         delete h;
@@ -231,6 +236,17 @@ ep_status ep_combine(ep_handle h, const void *expert_out, int64_t expert_out_row
     if (!aligned16(expert_out) || !aligned16(out)) return EP_ERR_INVALID_ARG;
     return ep::launch_combine(h, expert_out, expert_out_rows, topk_weights, topk_idx, layout, out,
                               static_cast<cudaStream_t>(stream));
+}
+
+ep_status ep_expert_layout(ep_handle h, const int32_t *topk_idx, const float *topk_weights,
+                           const ep_layout_out *layout, const ep_expert_layout_out *out, int64_t recv_rows,
+                           int64_t expert_rows_capacity, void *stream) {
+    if (!h || !topk_idx || !topk_weights || !layout_ptrs_ok(layout) || !out || !out->recv_topk_idx ||
+        !out->recv_topk_weights || !out->recv_src_token || !out->expert_rows || !out->expert_count ||
+        recv_rows < 0 || expert_rows_capacity < 0)
+        return EP_ERR_INVALID_ARG;
+    return ep::launch_expert_layout(h, topk_idx, topk_weights, layout, out, recv_rows, expert_rows_capacity,
+                                    static_cast<cudaStream_t>(stream));
 }
 
 ep_status ep_cmd_log_get(ep_handle h, ep_cmd_log *out) {

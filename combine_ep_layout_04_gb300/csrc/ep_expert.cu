@@ -1,0 +1,274 @@
+// ep_expert.cu -- expert-major receive metadata of one EP layer (sm_103a).
+//
+// What it computes (UCCL-EP article s1: each token goes to the experts of its
+// top-k picks; the receiving rank runs those experts on the rows it got):
+//   per receive row n = recv_base[d] + token_slot[t][d]: the source token t,
+//   and the token's picks that live on rank d as local expert ids with their
+//   weights (-1 / 0 elsewhere);
+//   per expert e: the receive rows of its picks in token order, placed at
+//   expert_off[e] + j, and the count of its picks.
+//
+// How: one CTA per tile of 128 tokens (one token per thread), tiles handed
+// out in launch order by a ticket counter, so a tile's predecessors are
+// already running.  Per tile:
+//   1. each thread holds its token's K picks and weights in registers,
+//      checks them (range, no expert named twice), sets its bit in the tile's
+//      bitmask of each picked expert (shared memory, E x 4 words), and writes
+//      the metadata of each receive row the token owns (one row per rank it
+//      reaches; K-wide vector stores where K % 4 == 0);
+//   2. per expert column: the tile's count is the popcount of its mask;
+//      decoupled look-back (Merrill & Garland, "Single-pass Parallel Prefix
+//      Scan with Decoupled Look-back", 2016) over the preceding tiles gives
+//      the picks of that expert in earlier tokens.  All columns' aggregates
+//      are published before any look-back starts.  A descriptor is one 64-bit
+//      word {epoch:30 | flag:2 | value:32}; the epoch comes from the ticket,
+//      so nothing is reset between calls (CUDA-graph safe);
+//   3. each pick's position = expert_off[e] + earlier tiles + popcount of the
+//      mask bits of earlier tokens in this tile; expert_rows gets the pick's
+//      receive row there.
+// Reads T*K*8 (picks, weights) plus each pick's token_slot entry; writes
+// N*(8K + 4) + M*4 + E*4 bytes.
+#include "ep_internal.cuh"
+
+namespace ep {
+namespace {
+
+constexpr int kXTile = 128;
+constexpr int kXWords = kXTile / 32;      // mask words per expert (one per warp)
+constexpr unsigned kFull = 0xffffffffu;
+constexpr uint32_t kXFlagAggregate = 1, kXFlagPrefix = 2;
+
+struct ExpertParams {
+    const int32_t *topk_idx;
+    const float *topk_weights;
+    const int32_t *token_slot;
+    const int32_t *recv_base;
+    const int32_t *expert_off;
+    ep_expert_layout_out out;
+    DevState dev;
+    int64_t T, recv_rows, rows_cap;
+    uint64_t timeout_ns;
+    int R, E, K, Er;
+    int tiles;
+    int vec4;              // K % 4 == 0 and the row outputs are 16-byte aligned
+};
+
+__device__ __forceinline__ unsigned long long pack_xdesc(uint32_t epoch, uint32_t flag, uint32_t value) {
+    return (static_cast<unsigned long long>(epoch) << 34) | (static_cast<unsigned long long>(flag) << 32) | value;
+}
+
+template <int KMAX>
+__global__ void __launch_bounds__(kXTile) expert_layout_kernel(const ExpertParams p) {
+    extern __shared__ __align__(16) uint32_t s_mask[];    // [E][kXWords], then s_excl[E]
+    __shared__ unsigned long long s_ticket;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int R = p.R, E = p.E, K = p.K, Er = p.Er;
+    int *s_excl = reinterpret_cast<int *>(s_mask + static_cast<size_t>(E) * kXWords);
+
+    if (tid == 0) s_ticket = atomicAdd(p.dev.xticket, 1ull);
+    for (int i = tid; i < E * kXWords; i += kXTile) s_mask[i] = 0u;
+    __syncthreads();
+    const unsigned long long ticket = s_ticket;
+    const int tile = static_cast<int>(ticket % static_cast<unsigned long long>(p.tiles));
+    const uint32_t epoch = static_cast<uint32_t>((ticket / p.tiles) % ((1u << 30) - 1u)) + 1u;
+    const int64_t t = static_cast<int64_t>(tile) * kXTile + tid;
+    const bool valid = t < p.T;
+
+    // 1. picks and weights in registers; -1 marks "no pick" and bad picks
+    int pk[KMAX];
+    float wk[KMAX];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+        pk[k] = -1;
+        wk[k] = 0.0f;
+        if (valid && k < K) {
+            int e = __ldg(p.topk_idx + t * K + k);
+            if (e < -1 || e >= E) {
+                set_error(p.dev.err, EP_ERR_INVALID_ARG);
+                e = -1;
+            }
+#pragma unroll
+            for (int k2 = 0; k2 < k; ++k2)
+                if (e >= 0 && pk[k2] == e) {
+                    set_error(p.dev.err, EP_ERR_INVALID_ARG);
+                    e = -1;
+                }
+            pk[k] = e;
+            wk[k] = __ldg(p.topk_weights + t * K + k);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+        if (pk[k] >= 0) atomicOr(&s_mask[pk[k] * kXWords + warp], 1u << lane);
+
+    // per-row metadata: one receive row per rank the token reaches, written
+    // when its first pick on that rank comes up
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+        if (pk[k] < 0) continue;
+        const int d = pk[k] / Er;
+        bool first = true;
+#pragma unroll
+        for (int k2 = 0; k2 < k; ++k2)
+            if (pk[k2] >= 0 && pk[k2] / Er == d) first = false;
+        if (!first) continue;
+        const int slot = __ldg(p.token_slot + t * R + d);
+        const int64_t n = static_cast<int64_t>(__ldg(p.recv_base + d)) + slot;
+        if (slot < 0 || n < 0) {
+            set_error(p.dev.err, EP_ERR_INVALID_ARG);    // layout of another routing
+            continue;
+        }
+        if (n >= p.recv_rows) {
+            set_error(p.dev.err, EP_ERR_CAPACITY);
+            continue;
+        }
+        p.out.recv_src_token[n] = static_cast<int32_t>(t);
+        const int lo = d * Er;
+        if (p.vec4) {
+            int4 *ri = reinterpret_cast<int4 *>(p.out.recv_topk_idx + n * K);
+            float4 *rw = reinterpret_cast<float4 *>(p.out.recv_topk_weights + n * K);
+#pragma unroll
+            for (int k4 = 0; k4 < KMAX; k4 += 4) {
+                if (k4 >= K) break;
+                int v[4];
+                float u[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int e = pk[k4 + j];
+                    const bool on = e >= 0 && e / Er == d;
+                    v[j] = on ? e - lo : -1;
+                    u[j] = on ? wk[k4 + j] : 0.0f;
+                }
+                ri[k4 / 4] = make_int4(v[0], v[1], v[2], v[3]);
+                rw[k4 / 4] = make_float4(u[0], u[1], u[2], u[3]);
+            }
+        } else {
+#pragma unroll
+            for (int k2 = 0; k2 < KMAX; ++k2) {
+                if (k2 >= K) break;
+                const int e = pk[k2];
+                const bool on = e >= 0 && e / Er == d;
+                p.out.recv_topk_idx[n * K + k2] = on ? e - lo : -1;
+                p.out.recv_topk_weights[n * K + k2] = on ? wk[k2] : 0.0f;
+            }
+        }
+    }
+    __syncthreads();
+
+    // 2. per expert column: publish every aggregate, then look back
+    unsigned long long *desc = p.dev.xdesc + static_cast<int64_t>(tile) * E;
+    for (int e = tid; e < E; e += kXTile) {
+        const uint32_t *m = s_mask + e * kXWords;
+        int agg = 0;
+#pragma unroll
+        for (int w = 0; w < kXWords; ++w) agg += __popc(m[w]);
+        s_excl[e] = agg;
+        st_relaxed(desc + e, pack_xdesc(epoch, tile == 0 ? kXFlagPrefix : kXFlagAggregate,
+                                         static_cast<uint32_t>(agg)));
+    }
+    const uint64_t t_start = globaltimer_ns();
+    for (int e = tid; e < E; e += kXTile) {
+        const int agg = s_excl[e];
+        int excl = 0;
+        if (tile > 0) {
+            int pred = tile - 1;
+            uint32_t spins = 0;
+            while (pred >= 0) {
+                const unsigned long long v = ld_relaxed(p.dev.xdesc + static_cast<int64_t>(pred) * E + e);
+                const uint32_t ep_v = static_cast<uint32_t>(v >> 34);
+                const uint32_t flag = static_cast<uint32_t>(v >> 32) & 3u;
+                if (ep_v == epoch && flag != 0u) {
+                    excl += static_cast<int>(static_cast<uint32_t>(v));
+                    if (flag == kXFlagPrefix) break;
+                    --pred;
+                    continue;
+                }
+                if ((++spins & 63u) == 0u) {
+                    if (globaltimer_ns() - t_start > p.timeout_ns) {
+                        set_error(p.dev.err, EP_ERR_TIMEOUT);
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+            }
+            st_relaxed(desc + e, pack_xdesc(epoch, kXFlagPrefix, static_cast<uint32_t>(excl + agg)));
+        }
+        s_excl[e] = excl;
+        if (tile == p.tiles - 1) p.out.expert_count[e] = excl + agg;
+    }
+    __syncthreads();
+
+    // 3. each pick's place in its expert's segment
+    const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+        const int e = pk[k];
+        if (e < 0) continue;
+        const uint32_t *m = s_mask + e * kXWords;
+        int pos = s_excl[e] + __popc(m[warp] & below);
+        for (int w = 0; w < warp; ++w) pos += __popc(m[w]);
+        const int64_t g = static_cast<int64_t>(__ldg(p.expert_off + e)) + pos;
+        const int d = e / Er;
+        const int slot = __ldg(p.token_slot + t * R + d);
+        if (slot < 0) continue;                           // reported above
+        if (g < 0 || g >= p.rows_cap) {
+            set_error(p.dev.err, EP_ERR_CAPACITY);
+            continue;
+        }
+        p.out.expert_rows[g] = __ldg(p.recv_base + d) + slot;
+    }
+}
+
+template <int KMAX>
+cudaError_t set_smem_limit(size_t bytes) {
+    return cudaFuncSetAttribute(expert_layout_kernel<KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(bytes));
+}
+
+size_t expert_smem_bytes(int E) { return static_cast<size_t>(E) * (kXWords + 1) * 4; }
+
+}  // namespace
+
+ep_status plan_expert_layout(ep_ctx *h) {
+    const int64_t T = static_cast<int64_t>(h->cfg.num_ranks) * h->cfg.tokens_per_rank;
+    h->xtiles = static_cast<int>((T + kXTile - 1) / kXTile);
+    const size_t smem = expert_smem_bytes(h->cfg.num_experts);
+    if (smem > 48 * 1024) {
+        const cudaError_t e = h->cfg.topk <= 8 ? set_smem_limit<8>(smem) : set_smem_limit<32>(smem);
+        if (e != cudaSuccess) return EP_ERR_CUDA;
+    }
+    return EP_OK;
+}
+
+ep_status launch_expert_layout(ep_ctx *h, const int32_t *topk_idx, const float *topk_weights,
+                               const ep_layout_out *lay, const ep_expert_layout_out *out,
+                               int64_t recv_rows, int64_t rows_cap, cudaStream_t st) {
+    ExpertParams p{};
+    p.topk_idx = topk_idx;
+    p.topk_weights = topk_weights;
+    p.token_slot = lay->token_slot;
+    p.recv_base = lay->recv_base;
+    p.expert_off = lay->expert_off;
+    p.out = *out;
+    p.dev = h->dev;
+    p.R = h->cfg.num_ranks;
+    p.E = h->cfg.num_experts;
+    p.K = h->cfg.topk;
+    p.Er = p.E / p.R;
+    p.T = static_cast<int64_t>(p.R) * h->cfg.tokens_per_rank;
+    p.recv_rows = recv_rows;
+    p.rows_cap = rows_cap;
+    p.timeout_ns = h->cfg.timeout_ns;
+    p.tiles = h->xtiles;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(out->recv_topk_idx) |
+                        reinterpret_cast<uintptr_t>(out->recv_topk_weights);
+    p.vec4 = (p.K % 4 == 0 && a % 16 == 0) ? 1 : 0;
+    const size_t smem = expert_smem_bytes(p.E);
+    if (p.K <= 8)
+        expert_layout_kernel<8><<<h->xtiles, kXTile, smem, st>>>(p);
+    else
+        expert_layout_kernel<32><<<h->xtiles, kXTile, smem, st>>>(p);
+    return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+}  // namespace ep

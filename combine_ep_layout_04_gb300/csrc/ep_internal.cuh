@@ -51,6 +51,9 @@ struct DevState {
     unsigned int *disp_gen;             // dispatch calls so far (tags `ready`)
     unsigned int *disp_done;            // CTAs finished in the current dispatch
     unsigned int *chunk_next;           // next chunk to hand to a copy CTA in the current dispatch
+    // expert layout scan
+    unsigned long long *xticket;        // expert-layout tiles handed out so far (all calls)
+    unsigned long long *xdesc;          // [xtiles * E] packed (epoch, flag, value)
 };
 
 // Layout kernel parameters.
@@ -123,6 +126,8 @@ struct ep_ctx {
     int64_t log_cap;
     // combine geometry
     int comb_grid, comb_threads;
+    // expert layout geometry
+    int xtiles;
 };
 
 namespace ep {
@@ -135,9 +140,13 @@ ep_status launch_dispatch(ep_ctx *h, const void *x, const ep_layout_out *lay, vo
 ep_status launch_combine(ep_ctx *h, const void *expert_out, int64_t eo_rows, const float *w,
                          const int32_t *topk_idx, const ep_layout_out *lay, void *out,
                          cudaStream_t st);
+ep_status launch_expert_layout(ep_ctx *h, const int32_t *topk_idx, const float *topk_weights,
+                               const ep_layout_out *lay, const ep_expert_layout_out *out,
+                               int64_t recv_rows, int64_t rows_cap, cudaStream_t st);
 // Dispatch geometry, decided once per handle.
 ep_status plan_dispatch(ep_ctx *h);
 ep_status plan_combine(ep_ctx *h);
+ep_status plan_expert_layout(ep_ctx *h);
 
 // ------------------------------------------------------------ device helpers
 #ifdef __CUDACC__

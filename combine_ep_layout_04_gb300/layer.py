@@ -45,6 +45,26 @@ class Layout:
         return d
 
 
+_EXPERT_FIELDS = ("recv_topk_idx", "recv_topk_weights", "recv_src_token", "expert_rows", "expert_count")
+
+
+@dataclasses.dataclass
+class ExpertLayout:
+    """Device outputs of ep_expert_layout (shapes in include/ep.h).
+    expert_rows holds T*K entries; the first sum(expert_count) are written."""
+    recv_topk_idx: torch.Tensor
+    recv_topk_weights: torch.Tensor
+    recv_src_token: torch.Tensor
+    expert_rows: torch.Tensor
+    expert_count: torch.Tensor
+
+    def struct(self) -> _ep.ep_expert_layout_out:
+        s = _ep.ep_expert_layout_out()
+        for f in _EXPERT_FIELDS:
+            setattr(s, f, getattr(self, f).data_ptr())
+        return s
+
+
 class _DevArray:
     """Exposes a library-owned device buffer to torch (zero copy)."""
 
@@ -137,6 +157,26 @@ class EpLayer:
             out = torch.empty((self.T, self.H), dtype=torch.bfloat16, device=self.device)
         _ep.ep_combine(self.handle, expert_out.data_ptr(), expert_out.shape[0], topk_weights.data_ptr(),
                        topk_idx.data_ptr(), lay.struct(), out.data_ptr(), _stream(self.device))
+        return out
+
+    def expert_layout(self, topk_idx: torch.Tensor, topk_weights: torch.Tensor, lay: Layout,
+                      out: ExpertLayout | None = None) -> ExpertLayout:
+        """ep_expert_layout: per receive row its source token and local picks
+        and weights; per expert its receive rows.  Needs N (a layout computed
+        with sync=True) unless `out` is given."""
+        assert topk_idx.dtype == torch.int32 and topk_idx.is_contiguous() and topk_idx.shape == (self.T, self.K)
+        assert topk_weights.dtype == torch.float32 and topk_weights.is_contiguous()
+        assert topk_weights.shape == (self.T, self.K)
+        if out is None:
+            if lay.n_recv is None:
+                raise ValueError("expert_layout needs `out` or a layout computed with sync=True")
+            N, K = lay.n_recv, self.K
+            i32 = dict(dtype=torch.int32, device=self.device)
+            out = ExpertLayout(torch.empty((N, K), **i32), torch.empty((N, K), dtype=torch.float32, device=self.device),
+                               torch.empty((N,), **i32), torch.empty((self.T * K,), **i32),
+                               torch.empty((self.E,), **i32))
+        _ep.ep_expert_layout(self.handle, topk_idx.data_ptr(), topk_weights.data_ptr(), lay.struct(), out.struct(),
+                             out.recv_src_token.shape[0], out.expert_rows.shape[0], _stream(self.device))
         return out
 
     # -- rings, status

@@ -118,6 +118,28 @@ typedef struct {
     int32_t *expert_off;
 } ep_layout_out;
 
+/* Caller-owned device outputs of ep_expert_layout: the expert-major view of
+ * the receive buffer that a rank's grouped expert step consumes.  N receive
+ * rows, K picks per token, E experts, Er = E / R experts per rank.
+ *  recv_topk_idx     [N, K] int32: pick k of the row's token as a local
+ *                    expert id (e - d*Er) if it lives on the row's rank d,
+ *                    else -1
+ *  recv_topk_weights [N, K] fp32:  topk_weights[t][k] where recv_topk_idx is
+ *                    not -1, else 0
+ *  recv_src_token    [N] int32:    the token t the row was copied from
+ *  expert_rows       [M] int32:    receive rows grouped by expert: expert e's
+ *                    rows are expert_rows[expert_off[e] + j], j <
+ *                    expert_count[e], in increasing row (= token) order;
+ *                    M = number of picks that are not -1 (at most T*K)
+ *  expert_count      [E] int32:    picks of expert e over all source ranks */
+typedef struct {
+    int32_t *recv_topk_idx;
+    float *recv_topk_weights;
+    int32_t *recv_src_token;
+    int32_t *expert_rows;
+    int32_t *expert_count;
+} ep_expert_layout_out;
+
 /* Library-owned view of the per-channel TransferCmd logs written by the ring
  * consumers during the last ep_dispatch.  Device pointers, valid until
  * ep_destroy; channel c's records are cmds[c * capacity_per_channel + i]
@@ -226,6 +248,31 @@ ep_status ep_dispatch(ep_handle h, const void *x, const ep_layout_out *layout, v
 ep_status ep_combine(ep_handle h, const void *expert_out, int64_t expert_out_rows,
                      const float *topk_weights, const int32_t *topk_idx,
                      const ep_layout_out *layout, void *out, void *stream);
+
+/* ep_expert_layout -- expert-major receive metadata ([UCCL-EP] s1: each
+ * token goes to the experts of its top-k picks, and the receiving rank runs
+ * those experts on the rows it received).  Needs only the layout, not the
+ * dispatched rows, so it may run on another stream while ep_dispatch moves
+ * the data.  One single-pass kernel over tiles of 128 tokens: per tile a
+ * bitmask of tokens per expert in shared memory, a decoupled-lookback scan
+ * down each expert column giving each pick's position in its expert's
+ * segment, and the per-row metadata written from the token's own picks.
+ *  topk_idx, topk_weights: device int32 / fp32 [T, K], the inputs of
+ *            ep_layout and ep_combine.  A pick outside [-1, E), or a token
+ *            naming one expert twice, sets EP_ERR_INVALID_ARG on the device
+ *            and that pick is skipped.
+ *  layout:   ep_layout's outputs for this routing (token_slot, recv_base and
+ *            expert_off are read on the device).
+ *  out:      caller-owned device outputs (all five pointers required).
+ *  recv_rows: rows of recv_topk_idx / recv_topk_weights / recv_src_token
+ *            (at least N); expert_rows_capacity: entries of expert_rows (at
+ *            least M; T*K always suffices).  A row or an entry beyond them
+ *            sets EP_ERR_CAPACITY on the device and is not written.
+ * The handle's scratch for this call grows as T*E/16 bytes (the lookback
+ * descriptors). */
+ep_status ep_expert_layout(ep_handle h, const int32_t *topk_idx, const float *topk_weights,
+                           const ep_layout_out *layout, const ep_expert_layout_out *out,
+                           int64_t recv_rows, int64_t expert_rows_capacity, void *stream);
 
 /* Device pointers of the TransferCmd logs (no synchronisation). */
 ep_status ep_cmd_log_get(ep_handle h, ep_cmd_log *out);

@@ -88,6 +88,7 @@ def test_null_handles_are_rejected(ep):
     assert ep.lib.ep_get_info(None, None) == ep.EP_ERR_INVALID_ARG
     assert ep.lib.ep_cmd_log_get(None, None) == ep.EP_ERR_INVALID_ARG
     assert ep.lib.ep_check_completion(None, 0, 0) == ep.EP_ERR_INVALID_ARG
+    assert ep.lib.ep_expert_layout(None, None, None, None, None, 0, 0, None) == ep.EP_ERR_INVALID_ARG
 
 
 def test_struct_sizes_match_the_header(ep):
@@ -95,3 +96,4 @@ def test_struct_sizes_match_the_header(ep):
     assert ctypes.sizeof(ep.ep_config) == 56
     assert ctypes.sizeof(ep.ep_layout_out) == 80
     assert ctypes.sizeof(ep.ep_ring_stats) == 48
+    assert ctypes.sizeof(ep.ep_expert_layout_out) == 40
