@@ -79,6 +79,8 @@ def _load():
         lib.oracle_combine.restype = i32
         lib.oracle_expert_layout.argtypes = [i32, i32, i32, i32, p, p, p, p, p, i64, p, p, p, p, p]
         lib.oracle_expert_layout.restype = i32
+        lib.oracle_signal_counts.argtypes = [i32, p, p]
+        lib.oracle_signal_counts.restype = None
         lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
         lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
         lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
@@ -218,6 +220,17 @@ def expert_layout(lay: dict, topk_idx: np.ndarray, topk_weights: np.ndarray, num
                                                            "recv_src_token", "expert_rows", "expert_count")])
     if rc != 0:
         raise OracleError(f"oracle_expert_layout: code {rc}")
+    return out
+
+
+def signal_counts(lay: dict) -> np.ndarray:
+    """Per destination rank, the signal value one dispatch leaves: one
+    increment per message landing there (NCCL GIN s2.2.2 signals, s2.1.2
+    put with SignalInc).  Returns uint64 [R]."""
+    msg = np.ascontiguousarray(lay["msg_count"], dtype=np.int32)
+    R = msg.shape[0]
+    out = np.zeros((R,), np.uint64)
+    _load().oracle_signal_counts(R, _ptr(msg), _ptr(out))
     return out
 
 

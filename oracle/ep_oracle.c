@@ -390,3 +390,22 @@ int oracle_expert_layout(int R, int Tpr, int E, int K, const int32_t *topk_idx,
         }
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------------------- signals -- */
+
+/*
+ * Arrival signals ([GIN] s2.2.2 completion notification: a put may carry a
+ * signal increment that the destination reads as remote completion; s2.1.2
+ * put with SignalInc, then waitSignal on an expected value).  With one signal
+ * per destination rank, incremented once per message that lands there, a
+ * dispatch leaves
+ *   signal[d] = number of messages of that dispatch with dst_rank d
+ *             = sum over s of msg_count[s][d].
+ */
+void oracle_signal_counts(int R, const int32_t *msg_count, uint64_t *signal) {
+    for (int d = 0; d < R; ++d) {
+        uint64_t n = 0;
+        for (int s = 0; s < R; ++s) n += (uint64_t)msg_count[s * R + d];
+        signal[d] = n;
+    }
+}

@@ -134,3 +134,36 @@ def test_small_workload_rings_wrap():
     w, idx, wt, G, lay = _setup("small")
     per = oracle.channel_counts(lay, w.channels)
     assert G == 8 and np.all(per > 3 * w.ring_depth)
+
+
+# ------------------------------------------------------------------ signals
+
+@pytest.mark.parametrize("seed", range(12))
+def test_signal_counts_are_messages_per_destination(seed):
+    # one increment per message: the count of TransferCmds addressed to d,
+    # taken here from the brute-force descriptor list (built message by message)
+    rng = np.random.default_rng(3000 + seed)
+    R = int(rng.integers(1, 6))
+    Tpr = int(rng.integers(1, 10))
+    Er = int(rng.integers(1, 3))
+    E, K = R * Er, int(rng.integers(1, min(3, R * Er) + 1))
+    idx = np.stack([rng.permutation(E)[:K] for _ in range(R * Tpr)]).astype(np.int32)
+    G = int(rng.choice([1, 2, 8]))
+    lay = oracle.layout(R, Tpr, E, idx, G)
+    sig = oracle.signal_counts(lay)
+    chans = brute.descriptors(lay, 3, G, 16)
+    per_d = np.zeros(R, np.uint64)
+    for ch in chans:
+        for (d, _, _, _) in ch:
+            per_d[d] += 1
+    assert np.array_equal(sig, per_d)
+
+
+def test_signal_counts_worked_example(golden):
+    g = golden("layout_worked_example.txt")
+    R, Tpr, E, K = g["R"][0], g["tokens_per_rank"][0], g["E"][0], g["K"][0]
+    idx = np.array(g["topk_idx"], np.int32).reshape(R * Tpr, K)
+    # G=2: messages to rank 0: (s0,d0) 1 + (s1,d0) 1; to rank 1: (s0,d1) 1 + (s1,d1) 2
+    assert oracle.signal_counts(oracle.layout(R, Tpr, E, idx, 2)).tolist() == [2, 3]
+    # G=1: one message per row: the receive counts 4 and 5
+    assert oracle.signal_counts(oracle.layout(R, Tpr, E, idx, 1)).tolist() == g["recv_count"]
