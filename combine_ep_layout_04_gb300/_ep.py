@@ -89,6 +89,10 @@ _sigs = {
     "ep_combine": ([_h, _p, ctypes.c_int64, _p, _p, ctypes.POINTER(ep_layout_out), _p, _p], ctypes.c_int),
     "ep_expert_layout": ([_h, _p, _p, ctypes.POINTER(ep_layout_out), ctypes.POINTER(ep_expert_layout_out),
                           ctypes.c_int64, ctypes.c_int64, _p], ctypes.c_int),
+    "ep_signal_ptr": ([_h, ctypes.POINTER(ctypes.c_void_p)], ctypes.c_int),
+    "ep_signal_get": ([_h, ctypes.POINTER(ctypes.c_uint64), ctypes.c_int32], ctypes.c_int),
+    "ep_signal_reset": ([_h, _p], ctypes.c_int),
+    "ep_wait_signal": ([_h, ctypes.c_int32, ctypes.c_uint64, ctypes.c_uint64, _p, _p], ctypes.c_int),
     "ep_cmd_log_get": ([_h, ctypes.POINTER(ep_cmd_log)], ctypes.c_int),
     "ep_ring_stats_get": ([_h, ctypes.POINTER(ep_ring_stats), ctypes.c_int32], ctypes.c_int),
     "ep_check_completion": ([_h, ctypes.c_int32, ctypes.c_uint64], ctypes.c_int),
@@ -173,6 +177,26 @@ def ep_expert_layout(h, topk_idx_ptr: int, weights_ptr: int, layout: ep_layout_o
                      recv_rows: int, rows_cap: int, stream: int) -> None:
     check(lib.ep_expert_layout(h, topk_idx_ptr, weights_ptr, ctypes.byref(layout), ctypes.byref(out), recv_rows,
                                rows_cap, stream), "ep_expert_layout")
+
+
+def ep_signal_ptr(h) -> int:
+    p = ctypes.c_void_p()
+    check(lib.ep_signal_ptr(h, ctypes.byref(p)), "ep_signal_ptr")
+    return int(p.value)
+
+
+def ep_signal_get(h, n: int) -> list:
+    arr = (ctypes.c_uint64 * n)()
+    check(lib.ep_signal_get(h, arr, n), "ep_signal_get")
+    return [int(v) for v in arr]
+
+
+def ep_signal_reset(h, stream: int) -> None:
+    check(lib.ep_signal_reset(h, stream), "ep_signal_reset")
+
+
+def ep_wait_signal(h, dst_rank: int, expected: int, timeout_ns: int, status_ptr: int, stream: int) -> None:
+    check(lib.ep_wait_signal(h, dst_rank, expected, timeout_ns, status_ptr, stream), "ep_wait_signal")
 
 
 def ep_cmd_log_get(h) -> ep_cmd_log:

@@ -31,7 +31,8 @@ def _nvcc() -> str:
 
 def _inputs():
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
-    hdrs = sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h")))
+    hdrs = sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h")) +
+                  glob.glob(os.path.join(INCLUDE, "*.cuh")))
     return srcs, hdrs
 
 

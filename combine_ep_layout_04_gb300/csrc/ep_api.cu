@@ -21,6 +21,8 @@ int default_rows_per_msg(int hidden) { return 2 * hidden < 7 * 1024 ? 8 : 1; }
 
 ep_status cuda_ok(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
 
+constexpr uint64_t kMaxWaitNs = 10000000000ull;   // longest ep_wait_signal: 10 s
+
 bool layout_ptrs_ok(const ep_layout_out *o) {
     return o && o->num_tokens_per_expert && o->num_tokens_per_rank && o->is_token_in_rank && o->token_slot &&
            o->recv_off && o->send_off && o->msg_count && o->recv_count && o->recv_base && o->expert_off;
@@ -145,6 +147,7 @@ ep_status ep_create(const ep_config *cfg, ep_handle *out) {
     const size_t o_gen = cv.take<unsigned int>(1);
     const size_t o_ddone = cv.take<unsigned int>(1);
     const size_t o_cnext = cv.take<unsigned int>(1);
+    const size_t o_signal = cv.take<unsigned long long>(R);
     const size_t o_xticket = cv.take<unsigned long long>(1);
     const size_t o_xdesc = cv.take<unsigned long long>(static_cast<size_t>(h->xtiles) * E);
     h->alloc_bytes = cv.off;
@@ -176,6 +179,7 @@ ep_status ep_create(const ep_config *cfg, ep_handle *out) {
     d.disp_gen = reinterpret_cast<unsigned int *>(b + o_gen);
     d.disp_done = reinterpret_cast<unsigned int *>(b + o_ddone);
     d.chunk_next = reinterpret_cast<unsigned int *>(b + o_cnext);
+    d.signal = reinterpret_cast<unsigned long long *>(b + o_signal);
     d.xticket = reinterpret_cast<unsigned long long *>(b + o_xticket);
     d.xdesc = reinterpret_cast<unsigned long long *>(b + o_xdesc);
     if (cudaDeviceSynchronize() != cudaSuccess) {
@@ -247,6 +251,33 @@ ep_status ep_expert_layout(ep_handle h, const int32_t *topk_idx, const float *to
         return EP_ERR_INVALID_ARG;
     return ep::launch_expert_layout(h, topk_idx, topk_weights, layout, out, recv_rows, expert_rows_capacity,
                                     static_cast<cudaStream_t>(stream));
+}
+
+ep_status ep_signal_ptr(ep_handle h, const uint64_t **signals) {
+    if (!h || !signals) return EP_ERR_INVALID_ARG;
+    *signals = reinterpret_cast<const uint64_t *>(h->dev.signal);
+    return EP_OK;
+}
+
+ep_status ep_signal_get(ep_handle h, uint64_t *host_out, int32_t n) {
+    if (!h || !host_out || n < 0 || n > h->cfg.num_ranks) return EP_ERR_INVALID_ARG;
+    if (n == 0) return EP_OK;
+    if (cudaDeviceSynchronize() != cudaSuccess) return EP_ERR_CUDA;
+    return cuda_ok(cudaMemcpy(host_out, h->dev.signal, sizeof(uint64_t) * n, cudaMemcpyDeviceToHost));
+}
+
+ep_status ep_signal_reset(ep_handle h, void *stream) {
+    if (!h) return EP_ERR_INVALID_ARG;
+    return cuda_ok(cudaMemsetAsync(h->dev.signal, 0, sizeof(uint64_t) * h->cfg.num_ranks,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+ep_status ep_wait_signal(ep_handle h, int32_t dst_rank, uint64_t expected, uint64_t timeout_ns, int32_t *status_out,
+                         void *stream) {
+    if (!h || !status_out || dst_rank < 0 || dst_rank >= h->cfg.num_ranks || timeout_ns > kMaxWaitNs)
+        return EP_ERR_INVALID_ARG;
+    return ep::launch_wait_signal(h->dev.signal + dst_rank, expected, timeout_ns, status_out,
+                                  static_cast<cudaStream_t>(stream));
 }
 
 ep_status ep_cmd_log_get(ep_handle h, ep_cmd_log *out) {

@@ -646,6 +646,22 @@ __device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long
                 sleep = min(sleep * 2u, 64u);
             }
         }
+        // arrival signals: the group's messages to each destination have
+        // landed (their chunks' ready flags were acquired above) and are now
+        // posted -- one release add per destination and group
+        if (!failed) {
+            for (int i = 0; i < nd; ++i) {
+                int m = 0;
+                if (k < p.nchunks) {
+                    const int2 g = ranges[lane * ndmax + i];
+                    m = g.y - g.x;
+                }
+#pragma unroll
+                for (int o = 16; o; o >>= 1) m += __shfl_xor_sync(kFull, m, o);
+                __syncwarp();
+                if (lane == 0 && m > 0) red_add_release(p.dev.signal + c + i * C, static_cast<unsigned long long>(m));
+            }
+        }
         __syncwarp();
     }
     // statistics: one reduction per warp

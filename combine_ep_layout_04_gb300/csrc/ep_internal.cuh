@@ -51,6 +51,7 @@ struct DevState {
     unsigned int *disp_gen;             // dispatch calls so far (tags `ready`)
     unsigned int *disp_done;            // CTAs finished in the current dispatch
     unsigned int *chunk_next;           // next chunk to hand to a copy CTA in the current dispatch
+    unsigned long long *signal;         // [R] messages landed per destination rank (cumulative)
     // expert layout scan
     unsigned long long *xticket;        // expert-layout tiles handed out so far (all calls)
     unsigned long long *xdesc;          // [xtiles * E] packed (epoch, flag, value)
@@ -140,6 +141,8 @@ ep_status launch_dispatch(ep_ctx *h, const void *x, const ep_layout_out *lay, vo
 ep_status launch_combine(ep_ctx *h, const void *expert_out, int64_t eo_rows, const float *w,
                          const int32_t *topk_idx, const ep_layout_out *lay, void *out,
                          cudaStream_t st);
+ep_status launch_wait_signal(const unsigned long long *signal, unsigned long long expected,
+                             unsigned long long timeout_ns, int32_t *status, cudaStream_t st);
 ep_status launch_expert_layout(ep_ctx *h, const int32_t *topk_idx, const float *topk_weights,
                                const ep_layout_out *lay, const ep_expert_layout_out *out,
                                int64_t recv_rows, int64_t rows_cap, cudaStream_t st);
@@ -181,6 +184,9 @@ __device__ __forceinline__ void st_release(unsigned long long *p, unsigned long 
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void red_add_release(unsigned long long *p, unsigned long long v) {
+    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 __device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p) {
     unsigned int v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

@@ -179,6 +179,25 @@ class EpLayer:
                              out.recv_src_token.shape[0], out.expert_rows.shape[0], _stream(self.device))
         return out
 
+    # -- arrival signals
+    def signals(self) -> np.ndarray:
+        """signal[R] on the host (synchronises the device)."""
+        return np.array(_ep.ep_signal_get(self.handle, self.R), dtype=np.uint64)
+
+    def signal_tensor(self) -> torch.Tensor:
+        """The library-owned signal[R] as a uint64 device tensor (zero copy)."""
+        return torch.as_tensor(_DevArray(_ep.ep_signal_ptr(self.handle), (self.R,), "<u8"), device=self.device)
+
+    def reset_signals(self) -> None:
+        _ep.ep_signal_reset(self.handle, _stream(self.device))
+
+    def wait_signal(self, dst_rank: int, expected: int, timeout_ns: int, status: torch.Tensor) -> torch.Tensor:
+        """ep_wait_signal: enqueue a bounded wait; `status` (device int32 [1])
+        receives EP_OK or EP_ERR_NOT_READY."""
+        assert status.dtype == torch.int32 and status.device == self.device
+        _ep.ep_wait_signal(self.handle, dst_rank, expected, timeout_ns, status.data_ptr(), _stream(self.device))
+        return status
+
     # -- rings, status
     def cmd_log(self):
         """Per-channel TransferCmd logs of the last dispatch, as numpy records

@@ -274,6 +274,37 @@ ep_status ep_expert_layout(ep_handle h, const int32_t *topk_idx, const float *to
                            const ep_layout_out *layout, const ep_expert_layout_out *out,
                            int64_t recv_rows, int64_t expert_rows_capacity, void *stream);
 
+/* Arrival signals, one per destination rank ([GIN] s2.2.2 completion
+ * notification: remote-completion signals bumped by atomic adds, addressed by
+ * id; s2.1.2 put with SignalInc, then waitSignal on an expected value).
+ * signal[d] counts the messages of every ep_dispatch since ep_create,
+ * ep_reset or ep_signal_reset whose rows have landed in rank d's window; one
+ * dispatch adds sum_s msg_count[s][d].  Each increment is a GPU-scope release
+ * made after the message's rows were written.  include/ep_signal.cuh has the
+ * device-side read and bounded wait for a consumer's own kernels. */
+
+/* Device address of signal[R] (uint64), valid until ep_destroy. */
+ep_status ep_signal_ptr(ep_handle h, const uint64_t **signals);
+
+/* Copy signal[0, n) to host array out[n] (synchronises the device); n must
+ * not exceed the rank count. */
+ep_status ep_signal_get(ep_handle h, uint64_t *host_out, int32_t n);
+
+/* Zero every signal, ordered on `stream` ([GIN] s4.2.1: reset a signal
+ * before reuse). */
+ep_status ep_signal_reset(ep_handle h, void *stream);
+
+/* Enqueue on `stream` a one-thread kernel that polls signal[dst_rank] (acquire
+ * reads, 100 ns back-off) until it reaches `expected` or timeout_ns (at most
+ * 10 s) has passed, then writes EP_OK or EP_ERR_NOT_READY (the analogue of
+ * GIN_ERR_SIGNAL_PENDING) to the device int32 *status_out.  The handle's
+ * error word is not touched.  Wait for a dispatch enqueued before it (on this
+ * stream or ordered by an event): a wait running while the dispatch it waits
+ * for has not started can hold the SMs the dispatch needs, and then it runs
+ * out.  dst_rank outside [0, R) returns EP_ERR_INVALID_ARG. */
+ep_status ep_wait_signal(ep_handle h, int32_t dst_rank, uint64_t expected, uint64_t timeout_ns,
+                         int32_t *status_out, void *stream);
+
 /* Device pointers of the TransferCmd logs (no synchronisation). */
 ep_status ep_cmd_log_get(ep_handle h, ep_cmd_log *out);
 

@@ -89,6 +89,10 @@ def test_null_handles_are_rejected(ep):
     assert ep.lib.ep_cmd_log_get(None, None) == ep.EP_ERR_INVALID_ARG
     assert ep.lib.ep_check_completion(None, 0, 0) == ep.EP_ERR_INVALID_ARG
     assert ep.lib.ep_expert_layout(None, None, None, None, None, 0, 0, None) == ep.EP_ERR_INVALID_ARG
+    assert ep.lib.ep_signal_ptr(None, None) == ep.EP_ERR_INVALID_ARG
+    assert ep.lib.ep_signal_get(None, None, 0) == ep.EP_ERR_INVALID_ARG
+    assert ep.lib.ep_signal_reset(None, None) == ep.EP_ERR_INVALID_ARG
+    assert ep.lib.ep_wait_signal(None, 0, 0, 0, None, None) == ep.EP_ERR_INVALID_ARG
 
 
 def test_struct_sizes_match_the_header(ep):
