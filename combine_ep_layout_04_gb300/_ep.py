@@ -28,7 +28,8 @@ class ep_config(ctypes.Structure):
                 ("channels", ctypes.c_int32), ("ring_depth", ctypes.c_int32),
                 ("max_inflight", ctypes.c_int32), ("batch", ctypes.c_int32),
                 ("rows_per_msg", ctypes.c_int32), ("drain_batch", ctypes.c_int32),
-                ("debug_flags", ctypes.c_int32), ("timeout_ns", ctypes.c_uint64)]
+                ("debug_flags", ctypes.c_int32), ("num_sms", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("timeout_ns", ctypes.c_uint64)]
 
 
 class ep_transfer_cmd(ctypes.Structure):
@@ -67,7 +68,7 @@ class ep_info(ctypes.Structure):
 
 
 assert ctypes.sizeof(ep_transfer_cmd) == 32
-assert ctypes.sizeof(ep_config) == 56
+assert ctypes.sizeof(ep_config) == 64
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"libep.so is not built ({LIB_PATH}); run "
@@ -87,6 +88,10 @@ _sigs = {
     "ep_layout": ([_h, _p, ctypes.POINTER(ep_layout_out), ctypes.POINTER(ctypes.c_int64), _p], ctypes.c_int),
     "ep_dispatch": ([_h, _p, ctypes.POINTER(ep_layout_out), _p, ctypes.c_int64, _p], ctypes.c_int),
     "ep_combine": ([_h, _p, ctypes.c_int64, _p, _p, ctypes.POINTER(ep_layout_out), _p, _p], ctypes.c_int),
+    "ep_dispatch_ranks": ([_h, _p, ctypes.POINTER(ep_layout_out), _p, ctypes.c_int64, ctypes.c_int32,
+                           ctypes.c_int32, _p], ctypes.c_int),
+    "ep_combine_tokens": ([_h, _p, ctypes.c_int64, _p, _p, ctypes.POINTER(ep_layout_out), _p, ctypes.c_int64,
+                           ctypes.c_int64, _p], ctypes.c_int),
     "ep_expert_layout": ([_h, _p, _p, ctypes.POINTER(ep_layout_out), ctypes.POINTER(ep_expert_layout_out),
                           ctypes.c_int64, ctypes.c_int64, _p], ctypes.c_int),
     "ep_signal_ptr": ([_h, ctypes.POINTER(ctypes.c_void_p)], ctypes.c_int),
@@ -171,6 +176,18 @@ def ep_combine(h, expert_out_ptr: int, expert_out_rows: int, weights_ptr: int, t
                layout: ep_layout_out, out_ptr: int, stream: int) -> None:
     check(lib.ep_combine(h, expert_out_ptr, expert_out_rows, weights_ptr, topk_idx_ptr, ctypes.byref(layout),
                          out_ptr, stream), "ep_combine")
+
+
+def ep_dispatch_ranks(h, x_ptr: int, layout: ep_layout_out, recv_ptr: int, capacity_rows: int, src_begin: int,
+                      src_end: int, stream: int) -> None:
+    check(lib.ep_dispatch_ranks(h, x_ptr, ctypes.byref(layout), recv_ptr, capacity_rows, src_begin, src_end,
+                                stream), "ep_dispatch_ranks")
+
+
+def ep_combine_tokens(h, expert_out_ptr: int, expert_out_rows: int, weights_ptr: int, topk_idx_ptr: int,
+                      layout: ep_layout_out, out_ptr: int, t_begin: int, t_end: int, stream: int) -> None:
+    check(lib.ep_combine_tokens(h, expert_out_ptr, expert_out_rows, weights_ptr, topk_idx_ptr, ctypes.byref(layout),
+                                out_ptr, t_begin, t_end, stream), "ep_combine_tokens")
 
 
 def ep_expert_layout(h, topk_idx_ptr: int, weights_ptr: int, layout: ep_layout_out, out: ep_expert_layout_out,

@@ -79,6 +79,8 @@ ep_status ep_config_check(const ep_config *c) {
     if (c->rows_per_msg < 0 || c->rows_per_msg > 2047) return EP_ERR_INVALID_ARG;   // 11 bits in a ring slot
     if (c->drain_batch < 32 || c->drain_batch > 512 || c->drain_batch % 32 != 0) return EP_ERR_INVALID_ARG;
     if (c->debug_flags & ~EP_DEBUG_DISABLE_CONSUMER) return EP_ERR_INVALID_ARG;
+    if (c->num_sms < 0 || (c->num_sms > 0 && c->num_sms < c->channels + 1) || c->reserved != 0)
+        return EP_ERR_INVALID_ARG;
     const int64_t T = static_cast<int64_t>(c->num_ranks) * c->tokens_per_rank;
     const int64_t kmin = c->topk < c->num_ranks ? c->topk : c->num_ranks;
     // receive rows are counted in int32
@@ -226,20 +228,36 @@ ep_status ep_layout(ep_handle h, const int32_t *topk_idx, const ep_layout_out *o
     return EP_OK;
 }
 
+ep_status ep_dispatch_ranks(ep_handle h, const void *x, const ep_layout_out *layout, void *recv,
+                            int64_t recv_capacity_rows, int32_t src_begin, int32_t src_end, void *stream) {
+    if (!h || !x || !recv || !layout_ptrs_ok(layout) || recv_capacity_rows < 0) return EP_ERR_INVALID_ARG;
+    if (src_begin < 0 || src_end < src_begin || src_end > h->cfg.num_ranks) return EP_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(recv)) return EP_ERR_INVALID_ARG;
+    return ep::launch_dispatch(h, x, layout, recv, recv_capacity_rows, src_begin, src_end,
+                               static_cast<cudaStream_t>(stream));
+}
+
 ep_status ep_dispatch(ep_handle h, const void *x, const ep_layout_out *layout, void *recv,
                       int64_t recv_capacity_rows, void *stream) {
-    if (!h || !x || !recv || !layout_ptrs_ok(layout) || recv_capacity_rows < 0) return EP_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(recv)) return EP_ERR_INVALID_ARG;
-    return ep::launch_dispatch(h, x, layout, recv, recv_capacity_rows, static_cast<cudaStream_t>(stream));
+    return ep_dispatch_ranks(h, x, layout, recv, recv_capacity_rows, 0, h ? h->cfg.num_ranks : 0, stream);
+}
+
+ep_status ep_combine_tokens(ep_handle h, const void *expert_out, int64_t expert_out_rows, const float *topk_weights,
+                            const int32_t *topk_idx, const ep_layout_out *layout, void *out, int64_t t_begin,
+                            int64_t t_end, void *stream) {
+    if (!h || !expert_out || !topk_weights || !topk_idx || !layout_ptrs_ok(layout) || !out || expert_out_rows < 0)
+        return EP_ERR_INVALID_ARG;
+    const int64_t T = static_cast<int64_t>(h->cfg.num_ranks) * h->cfg.tokens_per_rank;
+    if (t_begin < 0 || t_end < t_begin || t_end > T) return EP_ERR_INVALID_ARG;
+    if (!aligned16(expert_out) || !aligned16(out)) return EP_ERR_INVALID_ARG;
+    return ep::launch_combine(h, expert_out, expert_out_rows, topk_weights, topk_idx, layout, out, t_begin, t_end,
+                              static_cast<cudaStream_t>(stream));
 }
 
 ep_status ep_combine(ep_handle h, const void *expert_out, int64_t expert_out_rows, const float *topk_weights,
                      const int32_t *topk_idx, const ep_layout_out *layout, void *out, void *stream) {
-    if (!h || !expert_out || !topk_weights || !topk_idx || !layout_ptrs_ok(layout) || !out || expert_out_rows < 0)
-        return EP_ERR_INVALID_ARG;
-    if (!aligned16(expert_out) || !aligned16(out)) return EP_ERR_INVALID_ARG;
-    return ep::launch_combine(h, expert_out, expert_out_rows, topk_weights, topk_idx, layout, out,
-                              static_cast<cudaStream_t>(stream));
+    const int64_t T = h ? static_cast<int64_t>(h->cfg.num_ranks) * h->cfg.tokens_per_rank : 0;
+    return ep_combine_tokens(h, expert_out, expert_out_rows, topk_weights, topk_idx, layout, out, 0, T, stream);
 }
 
 ep_status ep_expert_layout(ep_handle h, const int32_t *topk_idx, const float *topk_weights,

@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     const int K = p.K, R = p.R;
     const int64_t B = p.row_bytes;
 
-    for (int64_t t = warp0; t < p.T; t += nwarps) {
+    for (int64_t t = p.t_begin + warp0; t < p.t_end; t += nwarps) {
         int64_t row = -1;
         float w = 0.0f;
         if (lane < K) {
@@ -107,7 +107,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
 
 template <int KMAX, int SEGS>
 ep_status launch_k(ep_ctx *h, const CombineParams &p, cudaStream_t st) {
-    combine_kernel<KMAX, SEGS><<<h->comb_grid, kCombineThreads, 0, st>>>(p);
+    // one warp per token, at most the planned grid (grid-stride beyond it)
+    const int64_t warps_per_cta = kCombineThreads / 32;
+    const int64_t need = (p.t_end - p.t_begin + warps_per_cta - 1) / warps_per_cta;
+    const int grid = static_cast<int>(need < h->comb_grid ? need : h->comb_grid);
+    if (grid <= 0) return EP_OK;
+    combine_kernel<KMAX, SEGS><<<grid, kCombineThreads, 0, st>>>(p);
     return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }
 
@@ -117,14 +122,16 @@ ep_status plan_combine(ep_ctx *h) {
     const int64_t T = static_cast<int64_t>(h->cfg.num_ranks) * h->cfg.tokens_per_rank;
     const int64_t warps_per_cta = kCombineThreads / 32;
     const int64_t need = (T + warps_per_cta - 1) / warps_per_cta;
-    const int64_t cap = static_cast<int64_t>(h->sm_count) * 32;   // grid-stride beyond this
+    const int64_t sms = h->cfg.num_sms > 0 && h->cfg.num_sms < h->sm_count ? h->cfg.num_sms : h->sm_count;
+    const int64_t cap = sms * 32;   // grid-stride beyond this
     h->comb_grid = static_cast<int>(need < cap ? need : cap);
     h->comb_threads = kCombineThreads;
     return EP_OK;
 }
 
 ep_status launch_combine(ep_ctx *h, const void *expert_out, int64_t eo_rows, const float *w,
-                         const int32_t *topk_idx, const ep_layout_out *lay, void *out, cudaStream_t st) {
+                         const int32_t *topk_idx, const ep_layout_out *lay, void *out, int64_t t_begin,
+                         int64_t t_end, cudaStream_t st) {
     CombineParams p{};
     p.expert_out = static_cast<const uint8_t *>(expert_out);
     p.eo_rows = eo_rows;
@@ -136,6 +143,8 @@ ep_status launch_combine(ep_ctx *h, const void *expert_out, int64_t eo_rows, con
     p.dev = h->dev;
     p.R = h->cfg.num_ranks;
     p.T = static_cast<int64_t>(p.R) * h->cfg.tokens_per_rank;
+    p.t_begin = t_begin;
+    p.t_end = t_end;
     p.K = h->cfg.topk;
     p.E = h->cfg.num_experts;
     p.Er = p.E / p.R;

@@ -196,7 +196,7 @@ __device__ void copy_warp(const DispatchParams &p, uint8_t *smem, const SmemLayo
     auto draw = [&]() -> int {   // warp-uniform
         int k = -1;
         if (lane == 0) {
-            k = ahead < static_cast<unsigned>(p.nchunks) ? static_cast<int>(ahead) : -1;
+            k = ahead < static_cast<unsigned>(p.k1 - p.k0) ? p.k0 + static_cast<int>(ahead) : -1;
             if (k >= 0) ahead = atomicAdd(p.dev.chunk_next, 1u);
             ids[n_drawn % kIdSlots] = k;
         }
@@ -499,16 +499,16 @@ __device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long
     const int leader = (lane / p.batch) * p.batch;    // first lane of this lane's batch
     LaneStats st;
     bool failed = false;
-    const int ngroups = nd > 0 ? (p.nchunks + 31) / 32 : 0;
+    const int ngroups = nd > 0 ? (p.k1 - p.k0 + 31) / 32 : 0;
     uint64_t err_checked = globaltimer_ns();
     for (int grp = w; grp < ngroups && !failed; grp += kPosterWarps) {
-        const int k = grp * 32 + lane;
+        const int k = p.k0 + grp * 32 + lane;
         // The group's chunks complete within a few microseconds of each other
         // (they are drawn in order): wait for all of them, polling device
         // memory with a back-off, before posting -- so that while posting
         // the warp touches shared memory only and answers the ring at once.
         {
-            bool rdy = k >= p.nchunks;
+            bool rdy = k >= p.k1;
             const uint64_t tw = globaltimer_ns();
             unsigned nap = 256;
             while (!__all_sync(kFull, rdy)) {
@@ -530,7 +530,7 @@ __device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long
         {
             int total = 0;
             bool bad = false;
-            if (k < p.nchunks) {
+            if (k < p.k1) {
                 const int s = k / p.chunks_per_rank;
                 const int32_t *nt = p.dev.notice + static_cast<int64_t>(k) * 2 * R;
                 for (int i = 0; i < nd; ++i) {
@@ -582,7 +582,7 @@ __device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long
                     if (totals[mid] <= f0) lo = mid; else hi = mid - 1;
                 }
                 const int j = lo;
-                const int s = (grp * 32 + j) / p.chunks_per_rank;
+                const int s = (p.k0 + grp * 32 + j) / p.chunks_per_rank;
                 const int2 *rg = ranges + j * ndmax;
                 int f = f0 - totals[j], i = 0;
                 int2 g = rg[0];
@@ -652,7 +652,7 @@ __device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long
         if (!failed) {
             for (int i = 0; i < nd; ++i) {
                 int m = 0;
-                if (k < p.nchunks) {
+                if (k < p.k1) {
                     const int2 g = ranges[lane * ndmax + i];
                     m = g.y - g.x;
                 }
@@ -856,7 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
         for (int c = 0; c < p.C; ++c) {
             long long part = 0;
             for (int i = lane; i < p.R * p.R; i += 32)
-                if ((i % p.R) % p.C == c) part += __ldg(p.msg_count + i);
+                if ((i % p.R) % p.C == c && i / p.R >= p.s0 && i / p.R < p.s1) part += __ldg(p.msg_count + i);
             for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
             worst = max(worst, part);
             if (channel_cta && c == static_cast<int>(blockIdx.x)) mine = part;
@@ -948,7 +948,9 @@ ep_status plan_dispatch(ep_ctx *h) {
     // balances the load even when the batch is small, 8 to 32 tokens (the
     // meta warp takes one token per lane).
     const int64_t T = static_cast<int64_t>(R) * h->cfg.tokens_per_rank;
-    const int64_t copy_ctas = h->sm_count > C ? h->sm_count - C : 1;
+    const int64_t copy_ctas = h->disp_grid - C;
+    h->disp_grid = h->cfg.num_sms > 0 && h->cfg.num_sms < h->sm_count ? h->cfg.num_sms : h->sm_count;
+    if (h->disp_grid < C + 1) return EP_ERR_INVALID_ARG;   // at least one copy CTA
     int chunk_tokens = kChunkTokens;
     while (chunk_tokens > 8 && T < 4 * copy_ctas * chunk_tokens) chunk_tokens /= 2;
     int rows_per_item = 1, pieces = 1, piece_bytes = static_cast<int>(B);
@@ -996,13 +998,11 @@ ep_status plan_dispatch(ep_ctx *h) {
             cudaSuccess ||
         per_sm < 1)
         return EP_ERR_CUDA;
-    h->disp_grid = h->sm_count;
-    if (h->disp_grid < C + 1) return EP_ERR_INVALID_ARG;   // at least one copy CTA
     return EP_OK;
 }
 
 ep_status launch_dispatch(ep_ctx *h, const void *x, const ep_layout_out *lay, void *recv, int64_t cap_rows,
-                          cudaStream_t st) {
+                          int s_begin, int s_end, cudaStream_t st) {
     DispatchParams p{};
     p.x = static_cast<const uint8_t *>(x);
     p.recv = static_cast<uint8_t *>(recv);
@@ -1031,6 +1031,10 @@ ep_status launch_dispatch(ep_ctx *h, const void *x, const ep_layout_out *lay, vo
     p.chunks_per_rank = h->chunks_per_rank;
     p.chunk_tokens = h->chunk_tokens;
     p.nchunks = h->nchunks;
+    p.s0 = s_begin;
+    p.s1 = s_end;
+    p.k0 = s_begin * h->chunks_per_rank;
+    p.k1 = s_end * h->chunks_per_rank;
     p.rows_per_item = h->rows_per_item;
     p.pieces = h->pieces;
     p.piece_bytes = h->piece_bytes;

@@ -81,6 +81,8 @@ struct DispatchParams {
     uint64_t timeout_ns;
     int R, Tpr, C, D, max_inflight, batch, G, drain_batch, debug;
     int chunks_per_rank, nchunks;
+    int k0, k1;          // chunks of this call: those of source ranks [s0, s1)
+    int s0, s1;
     int chunk_tokens;    // tokens per chunk (8..32)
     int rows_per_item;   // tokens per item when a row fits a stage, else 1
     int pieces;          // pieces per row when it does not, else 1
@@ -101,6 +103,7 @@ struct CombineParams {
     uint8_t *out;
     DevState dev;
     int64_t T;
+    int64_t t_begin, t_end;   // tokens of this call
     int64_t row_bytes;
     int R, K, E, Er;
     int nseg;            // 16-byte segments per row
@@ -137,10 +140,10 @@ namespace ep {
 ep_status launch_layout(ep_ctx *h, const int32_t *topk_idx, const ep_layout_out *out,
                         cudaStream_t st);
 ep_status launch_dispatch(ep_ctx *h, const void *x, const ep_layout_out *lay, void *recv,
-                          int64_t cap_rows, cudaStream_t st);
+                          int64_t cap_rows, int s_begin, int s_end, cudaStream_t st);
 ep_status launch_combine(ep_ctx *h, const void *expert_out, int64_t eo_rows, const float *w,
                          const int32_t *topk_idx, const ep_layout_out *lay, void *out,
-                         cudaStream_t st);
+                         int64_t t_begin, int64_t t_end, cudaStream_t st);
 ep_status launch_wait_signal(const unsigned long long *signal, unsigned long long expected,
                              unsigned long long timeout_ns, int32_t *status, cudaStream_t st);
 ep_status launch_expert_layout(ep_ctx *h, const int32_t *topk_idx, const float *topk_weights,

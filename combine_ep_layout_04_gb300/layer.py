@@ -82,12 +82,12 @@ class EpLayer:
 
     def __init__(self, num_ranks: int, tokens_per_rank: int, hidden: int, num_experts: int, topk: int, *,
                  channels=None, ring_depth=None, max_inflight=None, batch=None, rows_per_msg=None,
-                 drain_batch=None, timeout_ns=None, debug_flags: int = 0, device=None):
+                 drain_batch=None, timeout_ns=None, num_sms=None, debug_flags: int = 0, device=None):
         self.device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
         cfg = _ep.ep_config_init(num_ranks, tokens_per_rank, hidden, num_experts, topk)
         for name, val in (("channels", channels), ("ring_depth", ring_depth), ("max_inflight", max_inflight),
                           ("batch", batch), ("rows_per_msg", rows_per_msg), ("drain_batch", drain_batch),
-                          ("timeout_ns", timeout_ns)):
+                          ("timeout_ns", timeout_ns), ("num_sms", num_sms)):
             if val is not None:
                 setattr(cfg, name, val)
         cfg.debug_flags = debug_flags
@@ -135,28 +135,40 @@ class EpLayer:
         out.n_recv = _ep.ep_layout(self.handle, topk_idx.data_ptr(), out.struct(), _stream(self.device), want_n=sync)
         return out
 
-    def dispatch(self, x: torch.Tensor, lay: Layout, recv: torch.Tensor | None = None) -> torch.Tensor:
-        """ep_dispatch.  x: bf16 [T, H].  Returns recv bf16 [capacity, H]."""
+    def dispatch(self, x: torch.Tensor, lay: Layout, recv: torch.Tensor | None = None,
+                 src_ranks: tuple[int, int] | None = None) -> torch.Tensor:
+        """ep_dispatch (ep_dispatch_ranks for src_ranks=(begin, end)).
+        x: bf16 [T, H].  Returns recv bf16 [capacity, H]."""
         assert x.dtype == torch.bfloat16 and x.is_contiguous() and x.shape == (self.T, self.H)
         if recv is None:
             if lay.n_recv is None:
                 raise ValueError("dispatch needs recv or a layout computed with sync=True")
             recv = torch.empty((lay.n_recv, self.H), dtype=torch.bfloat16, device=self.device)
         assert recv.dtype == torch.bfloat16 and recv.is_contiguous() and recv.shape[1] == self.H
-        _ep.ep_dispatch(self.handle, x.data_ptr(), lay.struct(), recv.data_ptr(), recv.shape[0],
-                        _stream(self.device))
+        if src_ranks is None:
+            _ep.ep_dispatch(self.handle, x.data_ptr(), lay.struct(), recv.data_ptr(), recv.shape[0],
+                            _stream(self.device))
+        else:
+            _ep.ep_dispatch_ranks(self.handle, x.data_ptr(), lay.struct(), recv.data_ptr(), recv.shape[0],
+                                  src_ranks[0], src_ranks[1], _stream(self.device))
         return recv
 
     def combine(self, expert_out: torch.Tensor, topk_weights: torch.Tensor, topk_idx: torch.Tensor, lay: Layout,
-                out: torch.Tensor | None = None) -> torch.Tensor:
-        """ep_combine.  expert_out: bf16 [rows, H]; topk_weights fp32 [T, K]."""
+                out: torch.Tensor | None = None, tokens: tuple[int, int] | None = None) -> torch.Tensor:
+        """ep_combine (ep_combine_tokens for tokens=(begin, end)).
+        expert_out: bf16 [rows, H]; topk_weights fp32 [T, K]."""
         assert expert_out.dtype == torch.bfloat16 and expert_out.is_contiguous() and expert_out.shape[1] == self.H
         assert topk_weights.dtype == torch.float32 and topk_weights.is_contiguous()
         assert topk_idx.dtype == torch.int32 and topk_idx.is_contiguous()
         if out is None:
             out = torch.empty((self.T, self.H), dtype=torch.bfloat16, device=self.device)
-        _ep.ep_combine(self.handle, expert_out.data_ptr(), expert_out.shape[0], topk_weights.data_ptr(),
-                       topk_idx.data_ptr(), lay.struct(), out.data_ptr(), _stream(self.device))
+        if tokens is None:
+            _ep.ep_combine(self.handle, expert_out.data_ptr(), expert_out.shape[0], topk_weights.data_ptr(),
+                           topk_idx.data_ptr(), lay.struct(), out.data_ptr(), _stream(self.device))
+        else:
+            _ep.ep_combine_tokens(self.handle, expert_out.data_ptr(), expert_out.shape[0], topk_weights.data_ptr(),
+                                  topk_idx.data_ptr(), lay.struct(), out.data_ptr(), tokens[0], tokens[1],
+                                  _stream(self.device))
         return out
 
     def expert_layout(self, topk_idx: torch.Tensor, topk_weights: torch.Tensor, lay: Layout,

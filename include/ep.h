@@ -63,12 +63,16 @@ typedef struct {
     int32_t num_experts;     /* E, a multiple of R; expert e lives on rank e / (E/R) */
     int32_t topk;            /* K, 1..32 */
     int32_t channels;        /* C, 1..64: rings; a message to rank d goes to ring d % C */
-    int32_t ring_depth;      /* D, power of two, 8..65536 slots per ring */
+    int32_t ring_depth;      /* D, power of two, 8..8192 slots per ring */
     int32_t max_inflight;    /* 8..D: producers wait while head - tail would exceed it */
     int32_t batch;           /* 1..8 commands reserved per head update */
     int32_t rows_per_msg;    /* G >= 1 rows per TransferCmd message; 0 = default rule */
     int32_t drain_batch;     /* 32 or a multiple of it: slots a consumer polls per step */
     int32_t debug_flags;     /* EP_DEBUG_* bits; 0 in normal use */
+    int32_t num_sms;         /* SMs the dispatch and combine grids may occupy, leaving
+                                the rest to concurrent work; 0 = all.  The dispatch
+                                needs at least channels + 1 */
+    int32_t reserved;        /* 0 */
     uint64_t timeout_ns;     /* limit of every device-side wait; 0 = 2 s */
 } ep_config;
 
@@ -248,6 +252,33 @@ ep_status ep_dispatch(ep_handle h, const void *x, const ep_layout_out *layout, v
 ep_status ep_combine(ep_handle h, const void *expert_out, int64_t expert_out_rows,
                      const float *topk_weights, const int32_t *topk_idx,
                      const ep_layout_out *layout, void *out, void *stream);
+
+/* Pieces of one layer, for overlap: the layer split into micro-batches so
+ * that the expert work on one piece, or the next layer, runs while another
+ * piece moves ([GIN] s3.1.2 expert computation overlapping communication; the
+ * GPU communication notes' "communication and compute overlap": combine
+ * overlapped with the next layer, fixed launch order in CUDA graphs).  With
+ * ep_config.num_sms below the SM count the dispatch and combine grids leave
+ * the remaining SMs to concurrent kernels.
+ *
+ * ep_dispatch_ranks -- ep_dispatch restricted to the tokens of source ranks
+ * [src_begin, src_end): their rows are copied to their receive rows, and the
+ * TransferCmds (and arrival signals) of the pairs (s, d) with s in the range
+ * are posted; other receive rows are not written.  The log then holds this
+ * call's commands.  Pieces that together cover [0, R) leave recv, the logged
+ * command multiset and the signals as one ep_dispatch does.  Calls on one
+ * handle must not overlap each other (they share the rings).
+ * 0 <= src_begin <= src_end <= R, else EP_ERR_INVALID_ARG. */
+ep_status ep_dispatch_ranks(ep_handle h, const void *x, const ep_layout_out *layout, void *recv,
+                            int64_t recv_capacity_rows, int32_t src_begin, int32_t src_end, void *stream);
+
+/* ep_combine_tokens -- ep_combine for tokens [t_begin, t_end) only: rows
+ * t_begin .. t_end-1 of out (still [T, H]) are written.
+ * 0 <= t_begin <= t_end <= T, else EP_ERR_INVALID_ARG. */
+ep_status ep_combine_tokens(ep_handle h, const void *expert_out, int64_t expert_out_rows,
+                            const float *topk_weights, const int32_t *topk_idx,
+                            const ep_layout_out *layout, void *out, int64_t t_begin, int64_t t_end,
+                            void *stream);
 
 /* ep_expert_layout -- expert-major receive metadata ([UCCL-EP] s1: each
  * token goes to the experts of its top-k picks, and the receiving rank runs

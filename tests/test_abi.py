@@ -58,6 +58,7 @@ def test_defaults_are_the_tuning_table(ep, golden):
     ("num_experts", 250), ("topk", 0), ("topk", 33), ("channels", 0), ("channels", 65),
     ("ring_depth", 1000), ("ring_depth", 4), ("ring_depth", 16384), ("max_inflight", 2048), ("max_inflight", 4), ("batch", 9),
     ("batch", 0), ("rows_per_msg", -1), ("drain_batch", 48), ("drain_batch", 1024), ("debug_flags", 4),
+    ("num_sms", -1), ("num_sms", 5), ("reserved", 1),
 ])
 def test_invalid_configs_are_rejected_on_the_host(ep, field, value):
     cfg = ep.ep_config_init(32, 128, 7168, 256, 8)
@@ -89,6 +90,8 @@ def test_null_handles_are_rejected(ep):
     assert ep.lib.ep_cmd_log_get(None, None) == ep.EP_ERR_INVALID_ARG
     assert ep.lib.ep_check_completion(None, 0, 0) == ep.EP_ERR_INVALID_ARG
     assert ep.lib.ep_expert_layout(None, None, None, None, None, 0, 0, None) == ep.EP_ERR_INVALID_ARG
+    assert ep.lib.ep_dispatch_ranks(None, None, None, None, 0, 0, 0, None) == ep.EP_ERR_INVALID_ARG
+    assert ep.lib.ep_combine_tokens(None, None, 0, None, None, None, None, 0, 0, None) == ep.EP_ERR_INVALID_ARG
     assert ep.lib.ep_signal_ptr(None, None) == ep.EP_ERR_INVALID_ARG
     assert ep.lib.ep_signal_get(None, None, 0) == ep.EP_ERR_INVALID_ARG
     assert ep.lib.ep_signal_reset(None, None) == ep.EP_ERR_INVALID_ARG
@@ -97,7 +100,7 @@ def test_null_handles_are_rejected(ep):
 
 def test_struct_sizes_match_the_header(ep):
     assert ctypes.sizeof(ep.ep_transfer_cmd) == 32
-    assert ctypes.sizeof(ep.ep_config) == 56
+    assert ctypes.sizeof(ep.ep_config) == 64
     assert ctypes.sizeof(ep.ep_layout_out) == 80
     assert ctypes.sizeof(ep.ep_ring_stats) == 48
     assert ctypes.sizeof(ep.ep_expert_layout_out) == 40

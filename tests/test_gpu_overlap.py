@@ -1,0 +1,152 @@
+"""Pieces of a layer for overlap: ep_dispatch_ranks over source-rank pieces
+and ep_combine_tokens over token pieces must together give exactly what the
+whole-layer calls give (receive rows, the TransferCmd multiset, the arrival
+signals, the combined output), each piece touching only its own rows; and an
+SM budget (ep_config.num_sms) must not change any result."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from _helpers import (bf16_tensor_to_bits, bf16_ulp_distance, check_dispatch_rows, compare_descriptors,
+                      compare_layout, oracle_combine_sample, workload_inputs)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    import combine_ep_layout_04_gb300  # noqa: F401  (fails loudly without libep.so)
+
+
+def make_layer(w, **kw):
+    from combine_ep_layout_04_gb300 import EpLayer
+    opts = dict(channels=w.channels, ring_depth=w.ring_depth, max_inflight=w.max_inflight,
+                rows_per_msg=w.rows_per_msg)
+    opts.update(kw)
+    return EpLayer(w.num_ranks, w.tokens_per_rank, w.hidden, w.num_experts, w.topk, **opts)
+
+
+def piece_bounds(n, cuts):
+    b = [0] + sorted(cuts) + [n]
+    return list(zip(b[:-1], b[1:]))
+
+
+@pytest.mark.parametrize("name,cuts", [("tiny", [1, 1, 3]), ("small", [5, 16, 17]), ("ll", [8, 24]),
+                                       ("skew", [3, 11])])
+def test_dispatch_pieces_equal_whole(name, cuts):
+    w = W.get(name)
+    idx, wt, x = workload_inputs(w, x_on_device=True)
+    layer = make_layer(w)
+    try:
+        topk = torch.from_numpy(idx).cuda()
+        lay = layer.layout(topk)
+        lay_o = oracle.layout(w.num_ranks, w.tokens_per_rank, w.num_experts, idx, layer.G)
+        compare_layout(lay.numpy(), lay_o)
+        N, R, Tpr = lay.n_recv, w.num_ranks, w.tokens_per_rank
+        recv = torch.full((N, w.hidden), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+        # receive row -> source rank, from the oracle's layout
+        ts = lay_o["token_slot"]
+        t_idx, d_idx = np.nonzero(ts >= 0)
+        row_src = np.empty(N, np.int64)
+        row_src[lay_o["recv_base"][d_idx].astype(np.int64) + ts[t_idx, d_idx]] = t_idx // Tpr
+        logs = [[] for _ in range(layer.cfg.channels)]
+        sig_want = np.zeros(R, np.uint64)
+        for (a, b) in piece_bounds(R, cuts):
+            layer.dispatch(x, lay, recv, src_ranks=(a, b))
+            torch.cuda.synchronize()
+            assert layer.device_status() == 0
+            for c, lg in enumerate(layer.cmd_log()):
+                logs[c].append(lg)
+            # only rows of the sources dispatched so far are written
+            untouched = (recv.view(torch.int16) == -1).all(dim=1).cpu().numpy()
+            assert np.array_equal(untouched, row_src >= b), (a, b)
+            sig_want += lay_o["msg_count"][a:b].sum(axis=0).astype(np.uint64)
+            assert np.array_equal(layer.signals(), sig_want)
+        check_dispatch_rows(recv, x, lay_o)
+        compare_descriptors([np.concatenate(l) for l in logs], lay_o, layer.cfg.channels, layer.G, 2 * w.hidden)
+        assert np.array_equal(layer.signals(), oracle.signal_counts(lay_o))
+    finally:
+        layer.close()
+
+
+@pytest.mark.parametrize("name", ["small", "ll"])
+def test_combine_pieces_equal_whole(name):
+    w = W.get(name)
+    idx, wt, x = workload_inputs(w, x_on_device=True)
+    layer = make_layer(w)
+    try:
+        topk = torch.from_numpy(idx).cuda()
+        wts = torch.from_numpy(wt).cuda()
+        lay = layer.layout(topk)
+        lay_o = oracle.layout(w.num_ranks, w.tokens_per_rank, w.num_experts, idx, layer.G)
+        eo = W.make_expert_out_torch(lay.n_recv, w.hidden, "cuda", w.seed)
+        whole = layer.combine(eo, wts, topk, lay)
+        T = w.num_tokens
+        out = torch.full_like(whole.view(torch.int16), -1).view(torch.bfloat16)
+        for (a, b) in piece_bounds(T, [0, 37, T // 2, T // 2, T - 1]):
+            layer.combine(eo, wts, topk, lay, out=out, tokens=(a, b))
+            torch.cuda.synchronize()
+            written = ~(out.view(torch.int16) == -1).all(dim=1).cpu().numpy()
+            assert written[:b].all() and not written[b:].any()
+        assert layer.device_status() == 0
+        assert torch.equal(out.view(torch.int16), whole.view(torch.int16))
+        rng = np.random.default_rng(3)
+        tokens = np.unique(np.concatenate([[0, T - 1], rng.choice(T, 128, replace=False)]))
+        ref = oracle_combine_sample(lay_o, idx, wt, w.experts_per_rank, eo, tokens)
+        got = bf16_tensor_to_bits(out[torch.from_numpy(tokens).cuda()])
+        assert bf16_ulp_distance(got, ref).max(initial=0) <= 1
+    finally:
+        layer.close()
+
+
+@pytest.mark.parametrize("num_sms", [9, 40, 100])
+def test_sm_budget_keeps_results(num_sms):
+    w = W.get("small")
+    idx, wt, x = workload_inputs(w, x_on_device=True)
+    layer = make_layer(w, num_sms=num_sms)
+    try:
+        assert layer.info["dispatch_grid"] == num_sms
+        topk = torch.from_numpy(idx).cuda()
+        wts = torch.from_numpy(wt).cuda()
+        lay = layer.layout(topk)
+        lay_o = oracle.layout(w.num_ranks, w.tokens_per_rank, w.num_experts, idx, layer.G)
+        recv = layer.dispatch(x, lay)
+        torch.cuda.synchronize()
+        assert layer.device_status() == 0
+        check_dispatch_rows(recv, x, lay_o)
+        compare_descriptors(layer.cmd_log(), lay_o, layer.cfg.channels, layer.G, 2 * w.hidden)
+        out = layer.combine(recv, wts, topk, lay)
+        torch.cuda.synchronize()
+        T = w.num_tokens
+        tokens = np.arange(0, T, 97)
+        ref = oracle_combine_sample(lay_o, idx, wt, w.experts_per_rank, recv, tokens)
+        got = bf16_tensor_to_bits(out[torch.from_numpy(tokens).cuda()])
+        assert bf16_ulp_distance(got, ref).max(initial=0) <= 1
+    finally:
+        layer.close()
+
+
+def test_bad_pieces_are_rejected_on_the_host():
+    from combine_ep_layout_04_gb300 import _ep
+    w = W.get("tiny")
+    idx, wt, x = workload_inputs(w, x_on_device=True)
+    layer = make_layer(w)
+    try:
+        topk = torch.from_numpy(idx).cuda()
+        wts = torch.from_numpy(wt).cuda()
+        lay = layer.layout(topk)
+        recv = torch.empty((lay.n_recv, w.hidden), dtype=torch.bfloat16, device="cuda")
+        for rng_ in [(-1, 2), (3, 2), (0, w.num_ranks + 1)]:
+            with pytest.raises(_ep.EpError):
+                layer.dispatch(x, lay, recv, src_ranks=rng_)
+        for rng_ in [(-1, 2), (5, 4), (0, w.num_tokens + 1)]:
+            with pytest.raises(_ep.EpError):
+                layer.combine(recv, wts, topk, lay, tokens=rng_)
+        torch.cuda.synchronize()
+        assert layer.device_status() == 0
+    finally:
+        layer.close()
