@@ -63,7 +63,7 @@ class ep_info(ctypes.Structure):
     _fields_ = [("rows_per_msg", ctypes.c_int32), ("sm_count", ctypes.c_int32),
                 ("dispatch_grid", ctypes.c_int32), ("dispatch_stages", ctypes.c_int32),
                 ("dispatch_stage_bytes", ctypes.c_int32), ("combine_grid", ctypes.c_int32),
-                ("layout_tiles", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("layout_tiles", ctypes.c_int32), ("dispatch_chunk_tokens", ctypes.c_int32),
                 ("log_capacity_per_channel", ctypes.c_int64), ("scratch_bytes", ctypes.c_int64)]
 
 

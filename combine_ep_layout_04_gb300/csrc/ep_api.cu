@@ -365,6 +365,7 @@ ep_status ep_get_info(ep_handle h, ep_info *out) {
     out->dispatch_stage_bytes = h->stage_bytes;
     out->combine_grid = h->comb_grid;
     out->layout_tiles = h->tiles;
+    out->dispatch_chunk_tokens = h->chunk_tokens;
     out->log_capacity_per_channel = h->log_cap;
     out->scratch_bytes = static_cast<int64_t>(h->alloc_bytes);
     return EP_OK;

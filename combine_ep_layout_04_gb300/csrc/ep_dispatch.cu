@@ -855,8 +855,8 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
         long long worst = 0, mine = 0;
         for (int c = 0; c < p.C; ++c) {
             long long part = 0;
-            for (int i = lane; i < p.R * p.R; i += 32)
-                if ((i % p.R) % p.C == c && i / p.R >= p.s0 && i / p.R < p.s1) part += __ldg(p.msg_count + i);
+            for (int d = c; d < p.R; d += p.C)
+                for (int s = p.s0 + lane; s < p.s1; s += 32) part += __ldg(p.msg_count + s * p.R + d);
             for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
             worst = max(worst, part);
             if (channel_cta && c == static_cast<int>(blockIdx.x)) mine = part;
@@ -948,9 +948,9 @@ ep_status plan_dispatch(ep_ctx *h) {
     // balances the load even when the batch is small, 8 to 32 tokens (the
     // meta warp takes one token per lane).
     const int64_t T = static_cast<int64_t>(R) * h->cfg.tokens_per_rank;
-    const int64_t copy_ctas = h->disp_grid - C;
     h->disp_grid = h->cfg.num_sms > 0 && h->cfg.num_sms < h->sm_count ? h->cfg.num_sms : h->sm_count;
     if (h->disp_grid < C + 1) return EP_ERR_INVALID_ARG;   // at least one copy CTA
+    const int64_t copy_ctas = h->disp_grid - C;
     int chunk_tokens = kChunkTokens;
     while (chunk_tokens > 8 && T < 4 * copy_ctas * chunk_tokens) chunk_tokens /= 2;
     int rows_per_item = 1, pieces = 1, piece_bytes = static_cast<int>(B);

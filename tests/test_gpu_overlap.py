@@ -150,3 +150,29 @@ def test_bad_pieces_are_rejected_on_the_host():
         assert layer.device_status() == 0
     finally:
         layer.close()
+
+
+def expected_chunk_tokens(T, grid, C):
+    ct = 32
+    while ct > 8 and T < 4 * (grid - C) * ct:
+        ct //= 2
+    return ct
+
+
+@pytest.mark.parametrize("name,num_sms", [("ll", None), ("ht", None), ("small", None), ("ll", 40), ("tiny", 9)])
+def test_dispatch_plan_follows_the_grid(name, num_sms):
+    # small layers get smaller chunks so that every copy CTA has work; the
+    # rule uses the grid actually launched (all SMs, or the SM budget)
+    w = W.get(name)
+    layer = make_layer(w, num_sms=num_sms)
+    try:
+        info = layer.info
+        grid = info["sm_count"] if not num_sms else num_sms
+        assert info["dispatch_grid"] == grid
+        assert info["dispatch_chunk_tokens"] == expected_chunk_tokens(w.num_tokens, grid, layer.cfg.channels)
+        if name == "ll" and num_sms is None:
+            assert info["dispatch_chunk_tokens"] == 8
+        if name == "ht":
+            assert info["dispatch_chunk_tokens"] == 32
+    finally:
+        layer.close()
