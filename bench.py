@@ -212,6 +212,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens-per-rank", type=int, default=0,
                     help="override the workload's tokens per rank (smaller cases for profiler captures)")
+    ap.add_argument("--overlap", action="store_true",
+                    help="time dispatch -> stand-in expert GEMM -> combine over source-rank pieces, "
+                         "sequential against pipelined on three streams")
     ap.add_argument("--sweep", choices=["msg"], default=None,
                     help="msg: dispatch bandwidth against row and message size, one JSON line per point")
     args = ap.parse_args()
@@ -230,6 +233,8 @@ def main():
 
     if args.sweep:
         return run_sweep(args)
+    if args.overlap:
+        return run_overlap(args, w)
     if args.impl == "reference":
         return run_reference(args, w, world, rank)
 
@@ -381,6 +386,133 @@ def time_expert_layout(layer, topk, wts, lay, flush, st, peak, w, N, reps: int =
     t = float(np.median(times[3:]))
     return {"us": round(t * 1e6, 2), "bytes": nbytes, "GBps": round(nbytes / t / 1e9, 1),
             "frac": round(nbytes / t / 1e9 / peak, 4), "launches": reps}
+
+
+# ------------------------------------------------------------------- overlap
+def run_overlap(args, w, pieces: int = 4, gemm_cols: int = 256, reps: int = 10):
+    """Dispatch -> expert work -> combine of one layer, split into `pieces`
+    pieces of consecutive source ranks (ep_dispatch_ranks / ep_combine_tokens).
+    The expert work is a stand-in: one bf16 GEMM per piece, [N/pieces, H] x
+    [H, gemm_cols] with cuBLAS (torch.matmul), ordered after the piece's
+    dispatch and before its combine; combine reads the receive buffer
+    (identity expert), so the GEMM only occupies the GPU the way expert work
+    would.  Sequential: everything on one stream with every SM.  Pipelined:
+    dispatch pieces back to back on one stream, each piece's GEMM on a second
+    stream once the piece has landed, each piece's combine on a third once
+    its GEMM is done, with dispatch and combine limited to `num_sms` SMs.
+    One JSON line per SM budget."""
+    import torch
+
+    import workloads as W
+    from combine_ep_layout_04_gb300 import EpLayer
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    flush = torch.empty(2 * (getattr(props, "L2_cache_size", 0) or 128 * 2**20), dtype=torch.uint8, device=dev)
+    R, Tpr, H, T = w.num_ranks, w.tokens_per_rank, w.hidden, w.num_tokens
+    idx, wt = W.make_routing(w)
+    topk = torch.from_numpy(idx).to(dev)
+    wts = torch.from_numpy(wt).to(dev)
+    x = W.make_x_torch(w, dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed + 17)
+    Wg = (torch.randn((H, gemm_cols), device=dev, generator=g) * 0.02).to(torch.bfloat16)
+    bounds = [(i * R // pieces, (i + 1) * R // pieces) for i in range(pieces)]
+
+    def timed(fn, streams):
+        ts = []
+        for i in range(reps + 2):
+            flush.zero_()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            main = torch.cuda.current_stream(dev)
+            e0.record(main)
+            for s_ in streams:
+                s_.wait_event(e0)
+            fn()
+            for s_ in streams:
+                ev = torch.cuda.Event()
+                ev.record(s_)
+                main.wait_event(ev)
+            e1.record(main)
+            torch.cuda.synchronize(dev)
+            if i >= 2:
+                ts.append(e0.elapsed_time(e1))
+        return float(np.median(ts))
+
+    def make(num_sms):
+        L = EpLayer(R, Tpr, H, w.num_experts, w.topk, channels=w.channels, ring_depth=w.ring_depth,
+                    max_inflight=w.max_inflight, rows_per_msg=w.rows_per_msg, num_sms=num_sms, device=dev)
+        lay = L.layout(topk)
+        recv = torch.empty((lay.n_recv, H), dtype=torch.bfloat16, device=dev)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        return L, lay, recv, out
+
+    L, lay, recv, out = make(0)
+    N = lay.n_recv
+    rows = [(i * N // pieces, (i + 1) * N // pieces) for i in range(pieces)]
+    ys = [torch.empty((b - a, gemm_cols), dtype=torch.bfloat16, device=dev) for a, b in rows]
+
+    def gemm(i):
+        torch.matmul(recv[rows[i][0]:rows[i][1]], Wg, out=ys[i])
+
+    def comm_only():
+        for a, b in bounds:
+            L.dispatch(x, lay, recv, src_ranks=(a, b))
+        for a, b in bounds:
+            L.combine(recv, wts, topk, lay, out=out, tokens=(a * Tpr, b * Tpr))
+
+    def gemm_only():
+        for i in range(pieces):
+            gemm(i)
+
+    def sequential():
+        for a, b in bounds:
+            L.dispatch(x, lay, recv, src_ranks=(a, b))
+        gemm_only()
+        for a, b in bounds:
+            L.combine(recv, wts, topk, lay, out=out, tokens=(a * Tpr, b * Tpr))
+
+    t_comm = timed(comm_only, [])
+    t_gemm = timed(gemm_only, [])
+    t_seq = timed(sequential, [])
+    if L.device_status() != 0:
+        raise SystemExit(f"device status {L.device_status()} in the overlap run")
+    L.close()
+    flops = 2.0 * N * H * gemm_cols
+    for budget in (0, 120, 96, 64):
+        Lb, layb, recvb, outb = make(budget)
+        sG, sC = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+        def pipelined():
+            main = torch.cuda.current_stream(dev)
+            for i, (a, b) in enumerate(bounds):
+                Lb.dispatch(x, layb, recvb, src_ranks=(a, b))
+                ev = torch.cuda.Event()
+                ev.record(main)
+                sG.wait_event(ev)
+                with torch.cuda.stream(sG):
+                    torch.matmul(recvb[rows[i][0]:rows[i][1]], Wg, out=ys[i])
+                    eg = torch.cuda.Event()
+                    eg.record(sG)
+                sC.wait_event(eg)
+                with torch.cuda.stream(sC):
+                    Lb.combine(recvb, wts, topk, layb, out=outb, tokens=(a * Tpr, b * Tpr))
+
+        t_pipe = timed(pipelined, [sG, sC])
+        if Lb.device_status() != 0:
+            raise SystemExit(f"device status {Lb.device_status()} in the pipelined run")
+        if not torch.equal(outb.view(torch.int16), out.view(torch.int16)):
+            raise SystemExit("pipelined output differs from the sequential one")
+        Lb.close()
+        row = {"overlap": w.name, "pieces": pieces, "num_sms": budget or props.multi_processor_count,
+               "comm_ms": round(t_comm, 3), "gemm_ms": round(t_gemm, 3),
+               "gemm_tflops": round(flops / t_gemm / 1e9, 1), "sequential_ms": round(t_seq, 3),
+               "pipelined_ms": round(t_pipe, 3), "speedup": round(t_seq / t_pipe, 3),
+               "hidden_fraction": round((t_seq - t_pipe) / min(t_comm, t_gemm), 3),
+               "stand_in": f"bf16 GEMM [N/{pieces}, {H}] x [{H}, {gemm_cols}] per piece (cuBLAS)"}
+        print(json.dumps(row), flush=True)
 
 
 # --------------------------------------------------------------------- sweep
