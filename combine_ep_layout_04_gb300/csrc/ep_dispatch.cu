@@ -69,7 +69,7 @@
 namespace ep {
 namespace {
 
-constexpr int kThreads = 192;   // copy CTAs use warps 0-2; channel CTAs 0-5
+constexpr int kThreads = 320;   // copy CTAs use warps 0-2; channel CTAs 0-9
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMetaSlots = 3;       // destination lists in flight (copy CTAs)
 constexpr int kDoneSlots = 16;      // chunks stored but not yet reported complete
@@ -78,7 +78,10 @@ constexpr int kStoreLagItems = 2;   // items whose stores may still be in flight
 constexpr int kMaxPollRounds = 16;  // up to 512 slots examined per consumer step
 constexpr int kLogStage = 1024;     // staged records (16 bytes each) awaiting the logger
 constexpr uint64_t kErrCheckNs = 20000;   // idle loops read the device error word this often
-constexpr int kPosterWarpsMax = 4;        // shared-memory room for this many poster warps
+constexpr int kPosterWarpsMax = 8;        // shared-memory room for this many poster warps
+constexpr int kListPerLane = 8;           // commands a poster lane lists per posting pass
+constexpr int kMetaLoads = 8;             // int4 token_slot loads a meta lane keeps in flight
+constexpr int kNoticeLoads = 8;           // notice entries a poster lane keeps in flight
 
 // Shared words (u64) after rbase: abort flag; chunks complete (copy CTA) or
 // ring tail = retire point (channel CTA); poller stopped; ring base; dispatch
@@ -96,15 +99,20 @@ constexpr int kIdSlots = 32;   // chunk ids a copy CTA has drawn but not yet ret
 struct SmemLayout {
     int stage_off, meta_off, meta_slot_bytes, scratch_off, bar_off, total;
     __host__ __device__ static int ring_off(int R) { return ((12 * R * R) + 127) / 128 * 128; }
-    // poster ranges: per poster warp, 32 chunks x ceil(R/C) int2, then 32 totals
+    // poster ranges: per poster warp, 32 chunks x ceil(R/C) int2
     __host__ __device__ static int ranges_off(int R, int D) { return ring_off(R) + 16 * D + 16 * kLogStage; }
-    __host__ __device__ static int ranges_bytes_per_warp(int R, int C) { return 32 * ((R + C - 1) / C) * 8 + 33 * 4 + 12; }
+    __host__ __device__ static int ranges_bytes_per_warp(int R, int C) { return 32 * ((R + C - 1) / C) * 8; }
+    // poster lists: per poster warp, 32 x kListPerLane packed commands
+    __host__ __device__ static int lists_off(int R, int C, int D) {
+        return (ranges_off(R, D) + kPosterWarpsMax * ranges_bytes_per_warp(R, C) + 15) & ~15;
+    }
+    static constexpr int kListBytesPerWarp = 32 * kListPerLane * 16;
     __host__ __device__ SmemLayout(int R, int C, int D, int stage_bytes, int stages) {
         stage_off = 0;
         // channel CTAs keep the pair tables (3 x R x R ints) and their ring
         // (D slots of 16 bytes) where copy CTAs keep their stages
         const int stage_area = stage_bytes * stages,
-                  channel = ranges_off(R, D) + kPosterWarpsMax * ranges_bytes_per_warp(R, C);
+                  channel = lists_off(R, C, D) + kPosterWarpsMax * kListBytesPerWarp;
         meta_off = stage_area > channel ? stage_area : channel;
         meta_slot_bytes = ((32 * R + 33) + 3) / 4 * 16;   // dst[32*R] | pref[33]
         scratch_off = meta_off + meta_slot_bytes * kMetaSlots;
@@ -332,34 +340,50 @@ __device__ void build_meta(const DispatchParams &p, int k, const MetaSlot &ms, c
     int32_t *notice = p.dev.notice + static_cast<int64_t>(k) * 2 * R;
     int n = 0;
     int *dst = ms.dst + lane * R;
-    for (int d0 = 0; d0 < R; d0 += 4) {
-        int v[4] = {-1, -1, -1, -1};
-        if (valid) {
-            if (p.slot_vec) {
-                const int4 q = __ldg(reinterpret_cast<const int4 *>(p.token_slot + t * R + d0));
-                v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
-            } else {
-                for (int j = 0; j < 4 && d0 + j < R; ++j) v[j] = __ldg(p.token_slot + t * R + d0 + j);
+    // token_slot row of this lane's token, kMetaLoads x 4 destinations per
+    // batch: every load of a batch is issued before any is used, so a batch
+    // costs one memory round trip
+    for (int d00 = 0; d00 < R; d00 += 4 * kMetaLoads) {
+        int4 q[kMetaLoads];
+#pragma unroll
+        for (int b = 0; b < kMetaLoads; ++b) {
+            const int d0 = d00 + 4 * b;
+            q[b] = make_int4(-1, -1, -1, -1);
+            if (valid && d0 < R) {
+                if (p.slot_vec) {
+                    q[b] = __ldg(reinterpret_cast<const int4 *>(p.token_slot + t * R + d0));
+                } else {
+                    if (d0 + 0 < R) q[b].x = __ldg(p.token_slot + t * R + d0 + 0);
+                    if (d0 + 1 < R) q[b].y = __ldg(p.token_slot + t * R + d0 + 1);
+                    if (d0 + 2 < R) q[b].z = __ldg(p.token_slot + t * R + d0 + 2);
+                    if (d0 + 3 < R) q[b].w = __ldg(p.token_slot + t * R + d0 + 3);
+                }
             }
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int d = d0 + j;
-            if (d >= R) break;
-            const int sl = v[j];
-            if (sl >= 0) {
-                const int64_t row = static_cast<int64_t>(rbase[d]) + sl;
-                if (row >= 0 && row < p.cap_rows) {
-                    dst[n++] = static_cast<int>(row);
-                } else {
-                    set_error(p.dev.err, EP_ERR_CAPACITY);
+        for (int b = 0; b < kMetaLoads; ++b) {
+            const int d0 = d00 + 4 * b;
+            if (d0 >= R) break;
+            const int v[4] = {q[b].x, q[b].y, q[b].z, q[b].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int d = d0 + j;
+                if (d >= R) break;
+                const int sl = v[j];
+                if (sl >= 0) {
+                    const int64_t row = static_cast<int64_t>(rbase[d]) + sl;
+                    if (row >= 0 && row < p.cap_rows) {
+                        dst[n++] = static_cast<int>(row);
+                    } else {
+                        set_error(p.dev.err, EP_ERR_CAPACITY);
+                    }
                 }
-            }
-            const int lo = __reduce_min_sync(kFull, sl >= 0 ? sl : INT32_MAX);
-            const int hi = __reduce_max_sync(kFull, sl >= 0 ? sl : -1);
-            if (lane == (d & 31)) {
-                notice[2 * d] = lo == INT32_MAX ? -1 : lo;
-                notice[2 * d + 1] = hi;
+                const int lo = __reduce_min_sync(kFull, sl >= 0 ? sl : INT32_MAX);
+                const int hi = __reduce_max_sync(kFull, sl >= 0 ? sl : -1);
+                if (lane == (d & 31)) {
+                    notice[2 * d] = lo == INT32_MAX ? -1 : lo;
+                    notice[2 * d + 1] = hi;
+                }
             }
         }
     }
@@ -472,21 +496,23 @@ struct PairTables {
 // (one round trip for the group) and derives the messages the chunk
 // completes on ring c: those of pair (s, d) whose last row lies in the
 // chunk's rows [jlo, jhi] of the pair -- all earlier rows of the pair are in
-// earlier chunks.  The ranges go to shared memory.  Then the warp posts the
-// group's commands as one list, one command per lane and 32 a round: the
-// first lane of each batch of up to `batch` lanes reserves the batch's slots
-// with one atomicAdd on head, and each lane stores its slot as soon as
+// earlier chunks.  The ranges go to shared memory.  Then, in passes, every
+// lane writes its chunk's next commands (packed as a slot holds them) into
+// the warp's list -- a walk along its own ranges, no search -- and the warp
+// posts the list one command per lane, 32 a round: the first lane of each
+// batch of up to `batch` lanes reserves the batch's slots with one atomicAdd
+// on head, and each lane stores its slot as soon as
 // base + n - tail <= max_inflight (tail is the poller's retire point, in
 // shared memory).
-constexpr int kPosterWarps = 4;
-// Channel-CTA warps: warps 3 and 5 are the poller and the logger; the others
-// post.  A warp's SM sub-partition is its index mod 4, so the poller (warp 3)
-// has one to itself and answers the posters without waiting for issue slots.
+constexpr int kPosterWarps = 8;
+// Channel-CTA warps: warps 3 and 5 are the poller and the logger; the other
+// eight post.
 constexpr int kPollWarp = 3, kLogWarp = 5;
-__device__ __forceinline__ int poster_index(int warp) { return warp < kPollWarp ? warp : warp - 1; }
+static_assert(kThreads / 32 == kPosterWarps + 2, "one warp per poster, plus the poller and the logger");
+__device__ __forceinline__ int poster_index(int warp) { return warp - (warp > kPollWarp) - (warp > kLogWarp); }
 
 __device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long long *words, const PairTables &pt,
-                            unsigned long long *ring, int2 *ranges, int *totals) {
+                            unsigned long long *ring, int2 *ranges, unsigned long long *list) {
     const int lane = threadIdx.x & 31;
     const int R = p.R, C = p.C, G = p.G;
     const int nd = c < R ? (R - 1 - c) / C + 1 : 0;   // destinations d = c, c + C, ... on this ring
@@ -527,15 +553,26 @@ __device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long
             if (failed) break;
         }
         // this lane's chunk: messages [gb, ge) per destination of ring c
+        int total = 0;
         {
-            int total = 0;
             bool bad = false;
             if (k < p.k1) {
                 const int s = k / p.chunks_per_rank;
                 const int32_t *nt = p.dev.notice + static_cast<int64_t>(k) * 2 * R;
+                // kNoticeLoads destinations' notices in flight at once
+                int2 lhs[kNoticeLoads];
                 for (int i = 0; i < nd; ++i) {
                     const int d = c + i * C;
-                    const int2 lh = __ldcg(reinterpret_cast<const int2 *>(nt + 2 * d));
+                    if (i % kNoticeLoads == 0) {
+#pragma unroll
+                        for (int b = 0; b < kNoticeLoads; ++b)
+                            lhs[b] = i + b < nd ? __ldcg(reinterpret_cast<const int2 *>(nt + 2 * (d + b * C)))
+                                                : make_int2(-1, -1);
+                    }
+                    int2 lh = lhs[0];
+#pragma unroll
+                    for (int b = 1; b < kNoticeLoads; ++b)
+                        if (i % kNoticeLoads == b) lh = lhs[b];
                     int gb = 0, ge = 0;
                     if (lh.y >= 0) {
                         const int cnt = pt.cnt[s * R + d], r0 = pt.recv0[s * R + d];
@@ -555,101 +592,109 @@ __device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long
                 set_error(p.dev.err, EP_ERR_INVALID_ARG);
                 total = 0;
             }
-            // where each chunk's commands start in the group's list
-            int incl = total;
+            __syncwarp();
+        }
+        // Post the group's commands.  Each lane lists its own chunk's next
+        // commands (at most kListPerLane) into the warp's list, packed the way
+        // a slot holds them; the warp then posts the list, 32 (whole batches)
+        // a round, one command per lane.  A batch may span chunks.
+        int left = total;            // this lane's commands not yet listed
+        int ci = 0, cm = 0;          // cursor: destination index, message past gb
+        const int s_lane = k < p.k1 ? k / p.chunks_per_rank : 0;
+        while (!failed) {
+            const int take = min(left, kListPerLane);
+            int incl = take;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int y = __shfl_up_sync(kFull, incl, o);
                 if (lane >= o) incl += y;
             }
-            totals[lane] = incl - total;
-            if (lane == 31) totals[32] = incl;
+            const int ltot = __shfl_sync(kFull, incl, 31);
+            if (ltot == 0) break;
+            for (int q = 0, at = incl - take; q < take; ++q, ++at) {
+                int2 g = ranges[lane * ndmax + ci];
+                while (cm >= g.y - g.x) {
+                    ++ci;
+                    cm = 0;
+                    g = ranges[lane * ndmax + ci];
+                }
+                const int d = c + ci * C, pi = s_lane * R + d;
+                const int j0 = (g.x + cm) * G;
+                const int rows = min(G, pt.cnt[pi] - j0);
+                st_shared_v2(list + 2 * at,
+                             (static_cast<unsigned long long>(d) << 42) | (static_cast<unsigned long long>(rows) << 31) |
+                                 static_cast<unsigned long long>(pt.send0[pi] + j0),
+                             static_cast<unsigned long long>(pt.recv0[pi] + j0));
+                ++cm;
+            }
+            left -= take;
             __syncwarp();
-        }
-        // post the group's commands, 32 (whole batches) a round; a batch may
-        // span chunks
-        const int gtot = totals[32];
-        for (int r0 = 0; r0 < gtot && !failed; r0 += rs) {
-            const int nround = min(rs, gtot - r0);
-            const bool mine = lane < nround;
-            // command r0 + lane: chunk j (binary search), destination, message
-            unsigned long long w0 = 0ull, w1 = 0ull;
-            if (mine) {
-                const int f0 = r0 + lane;
-                int lo = 0, hi = 31;   // the last chunk j with totals[j] <= f0
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
-                    if (totals[mid] <= f0) lo = mid; else hi = mid - 1;
+            for (int r0 = 0; r0 < ltot && !failed; r0 += rs) {
+                const int nround = min(rs, ltot - r0);
+                const bool mine = lane < nround;
+                unsigned long long w0 = 0ull, w1 = 0ull;
+                if (mine) {
+                    const ulonglong2 v = ld_shared_v2(list + 2 * (r0 + lane));
+                    w0 = v.x;
+                    w1 = v.y;
                 }
-                const int j = lo;
-                const int s = (p.k0 + grp * 32 + j) / p.chunks_per_rank;
-                const int2 *rg = ranges + j * ndmax;
-                int f = f0 - totals[j], i = 0;
-                int2 g = rg[0];
-                while (f >= g.y - g.x) {
-                    f -= g.y - g.x;
-                    g = rg[++i];
-                }
-                const int d = c + i * C, m = g.x + f;
-                const int j0 = m * G;
-                const int rows = min(G, pt.cnt[s * R + d] - j0);
-                w0 = (static_cast<unsigned long long>(d) << 42) | (static_cast<unsigned long long>(rows) << 31) |
-                     static_cast<unsigned long long>(pt.send0[s * R + d] + j0);
-                w1 = static_cast<unsigned long long>(pt.recv0[s * R + d] + j0);
-            }
-            // batch leaders reserve; every lane learns its batch's base
-            const int n = mine ? min(p.batch, nround - leader) : 0;
-            unsigned long long base = 0ull;
-            if (mine && lane == leader) base = atomicAdd(head, static_cast<unsigned long long>(n));
-            base = __shfl_sync(kFull, base, leader);
-            const unsigned long long idx = base + static_cast<unsigned long long>(lane - leader);
-            bool pending = mine;
-            uint64_t t0 = globaltimer_ns();
-            unsigned sleep = 32;
-            unsigned long long stalls = 0;
-            while (true) {
-                if (pending) {
-                    const unsigned long long tail = ld_acquire_cta_shared(&words[kWProgress]);
-                    if (base + n - tail <= limit) {
-                        const unsigned long long lt = lap_tag(idx, p.lg_depth);
-                        st_shared_v2(ring + 2 * (idx & dmask), w0 | lt, w1 | lt);
-                        if (lane == leader) {
-                            st.batches += 1;
-                            st.max_batch = max(st.max_batch, static_cast<unsigned>(n));
-                            st.max_inflight = max(st.max_inflight, static_cast<unsigned>(base + n - tail));
-                            st.stalls += stalls;
+                // batch leaders reserve; every lane learns its batch's base
+                const int n = mine ? min(p.batch, nround - leader) : 0;
+                unsigned long long base = 0ull;
+                if (mine && lane == leader) base = atomicAdd(head, static_cast<unsigned long long>(n));
+                base = __shfl_sync(kFull, base, leader);
+                const unsigned long long idx = base + static_cast<unsigned long long>(lane - leader);
+                bool pending = mine;
+                uint64_t t0 = globaltimer_ns();
+                unsigned sleep = 32;
+                unsigned long long stalls = 0;
+                while (true) {
+                    if (pending) {
+                        const unsigned long long tail = ld_acquire_cta_shared(&words[kWProgress]);
+                        if (base + n - tail <= limit) {
+                            const unsigned long long lt = lap_tag(idx, p.lg_depth);
+                            st_shared_v2(ring + 2 * (idx & dmask), w0 | lt, w1 | lt);
+                            if (lane == leader) {
+                                st.batches += 1;
+                                st.max_batch = max(st.max_batch, static_cast<unsigned>(n));
+                                st.max_inflight = max(st.max_inflight, static_cast<unsigned>(base + n - tail));
+                                st.stalls += stalls;
+                            }
+                            pending = false;
+                        } else {
+                            ++stalls;
                         }
-                        pending = false;
-                    } else {
-                        ++stalls;
                     }
-                }
-                if (!__any_sync(kFull, pending)) break;
-                // waiting touches shared memory only; the device error word
-                // (an L2 round trip) is read every few tens of microseconds
-                bool give_up = false;
-                if (pending) {
-                    const uint64_t now = globaltimer_ns();
-                    if (now - t0 > p.timeout_ns) {
-                        set_error(p.dev.err, EP_ERR_TIMEOUT);
-                        give_up = true;
-                    } else if (now - err_checked > kErrCheckNs) {
-                        err_checked = now;
-                        give_up = read_error(p.dev.err) != 0;
+                    if (!__any_sync(kFull, pending)) break;
+                    // waiting touches shared memory only; the device error word
+                    // (an L2 round trip) is read every few tens of microseconds
+                    bool give_up = false;
+                    if (pending) {
+                        const uint64_t now = globaltimer_ns();
+                        if (now - t0 > p.timeout_ns) {
+                            set_error(p.dev.err, EP_ERR_TIMEOUT);
+                            give_up = true;
+                        } else if (now - err_checked > kErrCheckNs) {
+                            err_checked = now;
+                            give_up = read_error(p.dev.err) != 0;
+                        }
                     }
+                    if (__any_sync(kFull, give_up)) {
+                        failed = true;
+                        break;
+                    }
+                    __nanosleep(sleep);
+                    sleep = min(sleep * 2u, 64u);
                 }
-                if (__any_sync(kFull, give_up)) {
-                    failed = true;
-                    break;
-                }
-                __nanosleep(sleep);
-                sleep = min(sleep * 2u, 64u);
             }
+            __syncwarp();
         }
         // arrival signals: the group's messages to each destination have
         // landed (their chunks' ready flags were acquired above) and are now
-        // posted -- one release add per destination and group
+        // posted -- one fence per group, then one add per destination
         if (!failed) {
+            __syncwarp();
+            if (lane == 0) fence_acq_rel_gpu();
             for (int i = 0; i < nd; ++i) {
                 int m = 0;
                 if (k < p.k1) {
@@ -658,8 +703,7 @@ __device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long
                 }
 #pragma unroll
                 for (int o = 16; o; o >>= 1) m += __shfl_xor_sync(kFull, m, o);
-                __syncwarp();
-                if (lane == 0 && m > 0) red_add_release(p.dev.signal + c + i * C, static_cast<unsigned long long>(m));
+                if (lane == 0 && m > 0) red_add_relaxed(p.dev.signal + c + i * C, static_cast<unsigned long long>(m));
             }
         }
         __syncwarp();
@@ -901,9 +945,9 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
                 pt.send0 = pt.recv0 + p.R * p.R;
                 const int pw = poster_index(warp);
                 uint8_t *rb = smem + SmemLayout::ranges_off(p.R, p.D) + pw * SmemLayout::ranges_bytes_per_warp(p.R, p.C);
+                uint8_t *lb = smem + SmemLayout::lists_off(p.R, p.C, p.D) + pw * SmemLayout::kListBytesPerWarp;
                 poster_warp(p, c, pw, words, pt, reinterpret_cast<unsigned long long *>(smem + SmemLayout::ring_off(p.R)),
-                            reinterpret_cast<int2 *>(rb),
-                            reinterpret_cast<int *>(rb + 32 * ((p.R + p.C - 1) / p.C) * 8));
+                            reinterpret_cast<int2 *>(rb), reinterpret_cast<unsigned long long *>(lb));
             } else if (!(p.debug & EP_DEBUG_DISABLE_CONSUMER)) {
                 unsigned long long *ring = reinterpret_cast<unsigned long long *>(smem + SmemLayout::ring_off(p.R));
                 unsigned long long *stage = ring + 2 * p.D;
