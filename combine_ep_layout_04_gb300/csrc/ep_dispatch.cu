@@ -17,7 +17,7 @@
 //
 // How: one persistent cooperative kernel, one CTA per SM, in two kinds.
 //
-// Copy CTAs (all but the first C) move the rows.  Chunks of 8 to 32 tokens of
+// Copy CTAs (all but the first C) move the rows.  Chunks of 4 to 32 tokens of
 // one source rank (about four per copy CTA at most) are drawn from a
 // device-wide counter (so faster SMs take more);
 // three warps hand each chunk on through mbarriers and shared counters:
@@ -989,14 +989,14 @@ ep_status plan_dispatch(ep_ctx *h) {
     const int64_t B = 2ll * h->cfg.hidden;
     const int kTargetStage = 16384;
     // Chunk size: about four chunks per copy CTA, so that the dynamic draw
-    // balances the load even when the batch is small, 8 to 32 tokens (the
+    // balances the load even when the batch is small, 4 to 32 tokens (the
     // meta warp takes one token per lane).
     const int64_t T = static_cast<int64_t>(R) * h->cfg.tokens_per_rank;
     h->disp_grid = h->cfg.num_sms > 0 && h->cfg.num_sms < h->sm_count ? h->cfg.num_sms : h->sm_count;
     if (h->disp_grid < C + 1) return EP_ERR_INVALID_ARG;   // at least one copy CTA
     const int64_t copy_ctas = h->disp_grid - C;
     int chunk_tokens = kChunkTokens;
-    while (chunk_tokens > 8 && T < 4 * copy_ctas * chunk_tokens) chunk_tokens /= 2;
+    while (chunk_tokens > 4 && T < 4 * copy_ctas * chunk_tokens) chunk_tokens /= 2;
     int rows_per_item = 1, pieces = 1, piece_bytes = static_cast<int>(B);
     if (B <= kTargetStage) {
         rows_per_item = static_cast<int>(kTargetStage / B);

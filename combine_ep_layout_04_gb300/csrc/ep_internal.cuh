@@ -83,7 +83,7 @@ struct DispatchParams {
     int chunks_per_rank, nchunks;
     int k0, k1;          // chunks of this call: those of source ranks [s0, s1)
     int s0, s1;
-    int chunk_tokens;    // tokens per chunk (8..32)
+    int chunk_tokens;    // tokens per chunk (4..32)
     int rows_per_item;   // tokens per item when a row fits a stage, else 1
     int pieces;          // pieces per row when it does not, else 1
     int piece_bytes;     // bytes per piece (a multiple of 16)

@@ -177,7 +177,7 @@ typedef struct {
     int32_t dispatch_stage_bytes; /* bytes per stage */
     int32_t combine_grid;         /* CTAs of the combine kernel */
     int32_t layout_tiles;         /* token tiles of the layout scan */
-    int32_t dispatch_chunk_tokens; /* tokens per dispatch chunk: 32, halved down to 8
+    int32_t dispatch_chunk_tokens; /* tokens per dispatch chunk: 32, halved down to 4
                                       while the layer has < 4 chunks per copy CTA */
     int64_t log_capacity_per_channel;
     int64_t scratch_bytes;        /* device memory the handle allocated */

@@ -154,7 +154,7 @@ def test_bad_pieces_are_rejected_on_the_host():
 
 def expected_chunk_tokens(T, grid, C):
     ct = 32
-    while ct > 8 and T < 4 * (grid - C) * ct:
+    while ct > 4 and T < 4 * (grid - C) * ct:
         ct //= 2
     return ct
 
@@ -171,7 +171,7 @@ def test_dispatch_plan_follows_the_grid(name, num_sms):
         assert info["dispatch_grid"] == grid
         assert info["dispatch_chunk_tokens"] == expected_chunk_tokens(w.num_tokens, grid, layer.cfg.channels)
         if name == "ll" and num_sms is None:
-            assert info["dispatch_chunk_tokens"] == 8
+            assert info["dispatch_chunk_tokens"] == 4
         if name == "ht":
             assert info["dispatch_chunk_tokens"] == 32
     finally:
