@@ -107,6 +107,7 @@ struct CombineParams {
     int64_t row_bytes;
     int R, K, E, Er;
     int nseg;            // 16-byte segments per row
+    int nparts;          // work items per token (parts of its row)
 };
 
 }  // namespace ep
