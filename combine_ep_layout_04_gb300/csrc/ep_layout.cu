@@ -23,9 +23,12 @@
 //      is one 64-bit word {epoch:30 | flag:2 | value:32}; the epoch is derived
 //      from the ticket, so stale words from earlier calls are never taken and
 //      nothing has to be reset between calls (CUDA-graph safe);
-//   4. write token_slot (lane = column, coalesced) and, at each source rank's
-//      first token, the column prefix, from which the last tile derives the
-//      per-(s, d) counts and all the small scans.
+//   4. write, at each source rank's first token, the column prefix (from
+//      which the last tile derives the per-(s, d) counts and all the small
+//      scans) and add the tile's histogram; fence; count the tile done;
+//   5. write token_slot (lane = column, coalesced) -- after the fence, which
+//      therefore does not wait for these stores; the last tile to finish
+//      then runs the small scans.
 #include "ep_internal.cuh"
 
 namespace ep {
@@ -88,13 +91,26 @@ __device__ void finish_layout(const LayoutParams &p, int *s_work, int *s_tmp) {
     const int tid = threadIdx.x;
     const int R = p.R, E = p.E, G = p.G;
     const int32_t *P = p.dev.col_prefix;
-    // per-(s, d) counts, window offsets, message counts
-    for (int i = tid; i < R * R; i += kTile) {
-        const int s = i / R, d = i - s * R;
-        const int a = __ldcg(P + s * R + d);
-        const int c = __ldcg(P + (s + 1) * R + d) - a;
+    // per-(s, d) counts, window offsets, message counts: every load issued
+    // before the first store (P[i] and P[i + R] are the prefixes of (s, d)
+    // at the first tokens of ranks s and s + 1)
+    constexpr int kPairsPerThread = kMaxRanks * kMaxRanks / kTile;
+    int pa[kPairsPerThread], pb[kPairsPerThread];
+#pragma unroll
+    for (int q = 0; q < kPairsPerThread; ++q) {
+        const int i = tid + q * kTile;
+        if (i < R * R) {
+            pa[q] = __ldcg(P + i);
+            pb[q] = __ldcg(P + i + R);
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < kPairsPerThread; ++q) {
+        const int i = tid + q * kTile;
+        if (i >= R * R) break;
+        const int c = pb[q] - pa[q];
         p.out.num_tokens_per_rank[i] = c;
-        p.out.recv_off[i] = a;
+        p.out.recv_off[i] = pa[q];
         p.out.msg_count[i] = (c + G - 1) / G;
         s_work[i] = c;
     }
@@ -126,11 +142,18 @@ __device__ void finish_layout(const LayoutParams &p, int *s_work, int *s_tmp) {
     // copying the histogram out and clearing the scratch as it goes
     for (int e = tid; e < E; e += kTile) {
         int tot = 0;
-        for (int s = 0; s < R; ++s) {
-            const int v = __ldcg(p.dev.hist + static_cast<int64_t>(s) * E + e);
-            p.out.num_tokens_per_expert[static_cast<int64_t>(s) * E + e] = v;
-            p.dev.hist[static_cast<int64_t>(s) * E + e] = 0;
-            tot += v;
+        for (int s0 = 0; s0 < R; s0 += 8) {   // eight loads in flight, then their stores
+            int v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                v[q] = s0 + q < R ? __ldcg(p.dev.hist + static_cast<int64_t>(s0 + q) * E + e) : 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (s0 + q >= R) break;
+                p.out.num_tokens_per_expert[static_cast<int64_t>(s0 + q) * E + e] = v[q];
+                p.dev.hist[static_cast<int64_t>(s0 + q) * E + e] = 0;
+                tot += v[q];
+            }
         }
         s_work[e] = tot;
     }
@@ -279,20 +302,19 @@ __global__ void __launch_bounds__(kTile) layout_kernel(const LayoutParams p) {
     }
     __syncthreads();
 
-    // 4. token_slot, lane = column; column prefix at each rank's first token
+    // 4. the column prefix at the first token of each source rank that
+    //    starts in this tile, and the tile's histogram: the last tile reads
+    //    both, so they go out before the fence
 #pragma unroll
     for (int g = 0; g < kMaxRanks / 32; ++g) {
         const int d = g * 32 + lane;
         if (g >= ngroups || d >= R) continue;
         const unsigned bits = colbits[g];
         const int base = s_excl[d] + s_wcnt[warp][d];
-        for (int j = 0; j < 32; ++j) {
-            const int local = warp * 32 + j;
-            if (local >= nt) break;
-            const int64_t tt = t0 + local;
-            const int pre = base + __popc(bits & ((1u << j) - 1u));
-            p.out.token_slot[tt * R + d] = ((bits >> j) & 1u) ? pre : -1;
-            if (tt % Tpr == 0) p.dev.col_prefix[static_cast<int64_t>(tt / Tpr) * R + d] = pre;
+        for (int64_t s = (t0 + Tpr - 1) / Tpr; s * Tpr < t0 + nt; ++s) {
+            const int j = static_cast<int>(s * Tpr - t0) - warp * 32;
+            if (j < 0 || j >= 32) continue;
+            p.dev.col_prefix[s * R + d] = base + __popc(bits & ((1u << j) - 1u));
         }
     }
     if (smem_hist) {
@@ -303,10 +325,26 @@ __global__ void __launch_bounds__(kTile) layout_kernel(const LayoutParams p) {
         }
     }
 
-    // 5. the last tile to finish derives the small scans
+    // 5. count this tile done; the last one to finish derives the small scans
     __threadfence();
     __syncthreads();
     if (tid == 0) s_is_last = (atomicAdd(p.dev.done, 1u) == static_cast<unsigned>(p.tiles - 1));
+
+    // 6. token_slot, lane = column (nothing in this kernel reads it back, so
+    //    the fence above does not wait for these stores)
+#pragma unroll
+    for (int g = 0; g < kMaxRanks / 32; ++g) {
+        const int d = g * 32 + lane;
+        if (g >= ngroups || d >= R) continue;
+        const unsigned bits = colbits[g];
+        const int base = s_excl[d] + s_wcnt[warp][d];
+        for (int j = 0; j < 32; ++j) {
+            const int local = warp * 32 + j;
+            if (local >= nt) break;
+            const int64_t tt = t0 + local;
+            p.out.token_slot[tt * R + d] = ((bits >> j) & 1u) ? base + __popc(bits & ((1u << j) - 1u)) : -1;
+        }
+    }
     __syncthreads();
     if (!s_is_last) return;
     __threadfence();
