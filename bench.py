@@ -194,6 +194,23 @@ def cpu_oracle_rates(w, idx, wt, x_dev, eo_dev, budget_s: float = 12.0):
     return rates, full, note
 
 
+def slowest_rank(step_s: float, dist, device) -> float:
+    """The step time of the slowest replica (max over ranks); the local
+    value when not distributed."""
+    if dist is None:
+        return step_s
+    import torch
+    t = torch.tensor([step_s], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbps(world: int, bytes_per_replica: int, step_s: float) -> float:
+    """Whole-job GB/s: every replica moves the same bytes per step, and the
+    job's step lasts as long as its slowest replica's."""
+    return world * bytes_per_replica / step_s / 1e9
+
+
 def step_rate(full: dict, rates: dict) -> tuple[float, float]:
     """(GB/s over the whole step, seconds per step) at the given per-op rates."""
     secs = sum(full[k] / (rates[k] * 1e9) for k in full)
@@ -311,13 +328,9 @@ def main():
     t_disp = np.array([e[1].elapsed_time(e[2]) for e in evs]) * 1e-3
     t_comb = np.array([e[2].elapsed_time(e[3]) for e in evs]) * 1e-3
     t_step = t_layout + t_disp + t_comb
-    step_s = float(t_step.mean())
-    if dist:
-        tt = torch.tensor([step_s], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        step_s = float(tt.item())
+    step_s = slowest_rank(float(t_step.mean()), dist, dev)
     total_bytes = sum(ab.values())
-    value = world * total_bytes / step_s / 1e9
+    value = job_gbps(world, total_bytes, step_s)
 
     peak, peak_kind = read_peaks()
     per_op = {"layout": float(t_layout.mean()), "dispatch": float(t_disp.mean()), "combine": float(t_comb.mean())}
