@@ -12,10 +12,8 @@
 // out in launch order by a ticket counter, so a tile's predecessors are
 // already running.  Per tile:
 //   1. each thread holds its token's K picks and weights in registers,
-//      checks them (range, no expert named twice), sets its bit in the tile's
-//      bitmask of each picked expert (shared memory, E x 4 words), and writes
-//      the metadata of each receive row the token owns (one row per rank it
-//      reaches; K-wide vector stores where K % 4 == 0);
+//      checks them (range, no expert named twice), and sets its bit in the
+//      tile's bitmask of each picked expert (shared memory, E x 4 words);
 //   2. per expert column: the tile's count is the popcount of its mask;
 //      decoupled look-back (Merrill & Garland, "Single-pass Parallel Prefix
 //      Scan with Decoupled Look-back", 2016) over the preceding tiles gives
@@ -23,9 +21,11 @@
 //      are published before any look-back starts.  A descriptor is one 64-bit
 //      word {epoch:30 | flag:2 | value:32}; the epoch comes from the ticket,
 //      so nothing is reset between calls (CUDA-graph safe);
-//   3. each pick's position = expert_off[e] + earlier tiles + popcount of the
-//      mask bits of earlier tokens in this tile; expert_rows gets the pick's
-//      receive row there.
+//   3. the metadata of each receive row the token owns (one row per rank it
+//      reaches; K-wide vector stores where K % 4 == 0) -- after the look-back,
+//      so successors never wait on these stores -- and each pick's position =
+//      expert_off[e] + earlier tiles + popcount of the mask bits of earlier
+//      tokens in this tile; expert_rows gets the pick's receive row there.
 // Reads T*K*8 (picks, weights) plus each pick's token_slot entry; writes
 // N*(8K + 4) + M*4 + E*4 bytes.
 #include "ep_internal.cuh"
@@ -35,8 +35,7 @@ namespace {
 
 constexpr int kXTile = 128;
 constexpr int kXWords = kXTile / 32;      // mask words per expert (one per warp)
-constexpr unsigned kFull = 0xffffffffu;
-constexpr uint32_t kXFlagAggregate = 1, kXFlagPrefix = 2;
+constexpr int kPickBatch = 8;             // picks whose loads are in flight together
 
 struct ExpertParams {
     const int32_t *topk_idx;
@@ -52,10 +51,6 @@ struct ExpertParams {
     int tiles;
     int vec4;              // K % 4 == 0 and the row outputs are 16-byte aligned
 };
-
-__device__ __forceinline__ unsigned long long pack_xdesc(uint32_t epoch, uint32_t flag, uint32_t value) {
-    return (static_cast<unsigned long long>(epoch) << 34) | (static_cast<unsigned long long>(flag) << 32) | value;
-}
 
 template <int KMAX>
 __global__ void __launch_bounds__(kXTile) expert_layout_kernel(const ExpertParams p) {
@@ -101,58 +96,6 @@ __global__ void __launch_bounds__(kXTile) expert_layout_kernel(const ExpertParam
     for (int k = 0; k < KMAX; ++k)
         if (pk[k] >= 0) atomicOr(&s_mask[pk[k] * kXWords + warp], 1u << lane);
 
-    // per-row metadata: one receive row per rank the token reaches, written
-    // when its first pick on that rank comes up
-#pragma unroll
-    for (int k = 0; k < KMAX; ++k) {
-        if (pk[k] < 0) continue;
-        const int d = pk[k] / Er;
-        bool first = true;
-#pragma unroll
-        for (int k2 = 0; k2 < k; ++k2)
-            if (pk[k2] >= 0 && pk[k2] / Er == d) first = false;
-        if (!first) continue;
-        const int slot = __ldg(p.token_slot + t * R + d);
-        const int64_t n = static_cast<int64_t>(__ldg(p.recv_base + d)) + slot;
-        if (slot < 0 || n < 0) {
-            set_error(p.dev.err, EP_ERR_INVALID_ARG);    // layout of another routing
-            continue;
-        }
-        if (n >= p.recv_rows) {
-            set_error(p.dev.err, EP_ERR_CAPACITY);
-            continue;
-        }
-        p.out.recv_src_token[n] = static_cast<int32_t>(t);
-        const int lo = d * Er;
-        if (p.vec4) {
-            int4 *ri = reinterpret_cast<int4 *>(p.out.recv_topk_idx + n * K);
-            float4 *rw = reinterpret_cast<float4 *>(p.out.recv_topk_weights + n * K);
-#pragma unroll
-            for (int k4 = 0; k4 < KMAX; k4 += 4) {
-                if (k4 >= K) break;
-                int v[4];
-                float u[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int e = pk[k4 + j];
-                    const bool on = e >= 0 && e / Er == d;
-                    v[j] = on ? e - lo : -1;
-                    u[j] = on ? wk[k4 + j] : 0.0f;
-                }
-                ri[k4 / 4] = make_int4(v[0], v[1], v[2], v[3]);
-                rw[k4 / 4] = make_float4(u[0], u[1], u[2], u[3]);
-            }
-        } else {
-#pragma unroll
-            for (int k2 = 0; k2 < KMAX; ++k2) {
-                if (k2 >= K) break;
-                const int e = pk[k2];
-                const bool on = e >= 0 && e / Er == d;
-                p.out.recv_topk_idx[n * K + k2] = on ? e - lo : -1;
-                p.out.recv_topk_weights[n * K + k2] = on ? wk[k2] : 0.0f;
-            }
-        }
-    }
     __syncthreads();
 
     // 2. per expert column: publish every aggregate, then look back
@@ -163,7 +106,7 @@ __global__ void __launch_bounds__(kXTile) expert_layout_kernel(const ExpertParam
 #pragma unroll
         for (int w = 0; w < kXWords; ++w) agg += __popc(m[w]);
         s_excl[e] = agg;
-        st_relaxed(desc + e, pack_xdesc(epoch, tile == 0 ? kXFlagPrefix : kXFlagAggregate,
+        st_relaxed(desc + e, look_desc(epoch, tile == 0 ? kLookPrefix : kLookAggregate,
                                          static_cast<uint32_t>(agg)));
     }
     const uint64_t t_start = globaltimer_ns();
@@ -171,51 +114,100 @@ __global__ void __launch_bounds__(kXTile) expert_layout_kernel(const ExpertParam
         const int agg = s_excl[e];
         int excl = 0;
         if (tile > 0) {
-            int pred = tile - 1;
-            uint32_t spins = 0;
-            while (pred >= 0) {
-                const unsigned long long v = ld_relaxed(p.dev.xdesc + static_cast<int64_t>(pred) * E + e);
-                const uint32_t ep_v = static_cast<uint32_t>(v >> 34);
-                const uint32_t flag = static_cast<uint32_t>(v >> 32) & 3u;
-                if (ep_v == epoch && flag != 0u) {
-                    excl += static_cast<int>(static_cast<uint32_t>(v));
-                    if (flag == kXFlagPrefix) break;
-                    --pred;
-                    continue;
-                }
-                if ((++spins & 63u) == 0u) {
-                    if (globaltimer_ns() - t_start > p.timeout_ns) {
-                        set_error(p.dev.err, EP_ERR_TIMEOUT);
-                        break;
-                    }
-                    __nanosleep(64);
-                }
-            }
-            st_relaxed(desc + e, pack_xdesc(epoch, kXFlagPrefix, static_cast<uint32_t>(excl + agg)));
+            excl = lookback_excl(p.dev.xdesc, E, e, tile, epoch, t_start, p.timeout_ns, p.dev.err);
+            st_relaxed(desc + e, look_desc(epoch, kLookPrefix, static_cast<uint32_t>(excl + agg)));
         }
         s_excl[e] = excl;
         if (tile == p.tiles - 1) p.out.expert_count[e] = excl + agg;
     }
     __syncthreads();
 
-    // 3. each pick's place in its expert's segment
+    // 3. per pick, in batches of kPickBatch: first every load the batch
+    //    needs (the receive row of the pick's rank, its expert's offset) --
+    //    one round trip -- then the stores.
+    //    a. per-row metadata: one receive row per rank the token reaches,
+    //       written at its first pick on that rank (after the look-back, so
+    //       successors never wait on these stores);
+    //    b. the pick's place in its expert's segment: expert_off[e] + earlier
+    //       tiles + mask bits of earlier tokens in this tile.
     const unsigned below = (1u << lane) - 1u;
 #pragma unroll
-    for (int k = 0; k < KMAX; ++k) {
-        const int e = pk[k];
-        if (e < 0) continue;
-        const uint32_t *m = s_mask + e * kXWords;
-        int pos = s_excl[e] + __popc(m[warp] & below);
-        for (int w = 0; w < warp; ++w) pos += __popc(m[w]);
-        const int64_t g = static_cast<int64_t>(__ldg(p.expert_off + e)) + pos;
-        const int d = e / Er;
-        const int slot = __ldg(p.token_slot + t * R + d);
-        if (slot < 0) continue;                           // reported above
-        if (g < 0 || g >= p.rows_cap) {
-            set_error(p.dev.err, EP_ERR_CAPACITY);
-            continue;
+    for (int k0 = 0; k0 < KMAX; k0 += kPickBatch) {
+        int64_t row[kPickBatch];
+        int eoff[kPickBatch];
+#pragma unroll
+        for (int b = 0; b < kPickBatch; ++b) {
+            const int e = pk[k0 + b];
+            row[b] = -1;
+            eoff[b] = 0;
+            if (e >= 0) {
+                const int d = e / Er;
+                const int slot = __ldg(p.token_slot + t * R + d);
+                row[b] = slot >= 0 ? static_cast<int64_t>(__ldg(p.recv_base + d)) + slot : -1;
+                eoff[b] = __ldg(p.expert_off + e);
+            }
         }
-        p.out.expert_rows[g] = __ldg(p.recv_base + d) + slot;
+#pragma unroll
+        for (int b = 0; b < kPickBatch; ++b) {
+            const int k = k0 + b;
+            const int e = pk[k];
+            if (e < 0) continue;
+            const int d = e / Er;
+            const int64_t n = row[b];
+            if (n < 0) {
+                set_error(p.dev.err, EP_ERR_INVALID_ARG);    // layout of another routing
+                continue;
+            }
+            bool first = true;
+#pragma unroll
+            for (int k2 = 0; k2 < k; ++k2)
+                if (pk[k2] >= 0 && pk[k2] / Er == d) first = false;
+            if (first) {
+                if (n >= p.recv_rows) {
+                    set_error(p.dev.err, EP_ERR_CAPACITY);
+                } else {
+                    p.out.recv_src_token[n] = static_cast<int32_t>(t);
+                    const int lo = d * Er;
+                    if (p.vec4) {
+                        int4 *ri = reinterpret_cast<int4 *>(p.out.recv_topk_idx + n * K);
+                        float4 *rw = reinterpret_cast<float4 *>(p.out.recv_topk_weights + n * K);
+#pragma unroll
+                        for (int k4 = 0; k4 < KMAX; k4 += 4) {
+                            if (k4 >= K) break;
+                            int v[4];
+                            float u[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const int ej = pk[k4 + j];
+                                const bool on = ej >= 0 && ej / Er == d;
+                                v[j] = on ? ej - lo : -1;
+                                u[j] = on ? wk[k4 + j] : 0.0f;
+                            }
+                            ri[k4 / 4] = make_int4(v[0], v[1], v[2], v[3]);
+                            rw[k4 / 4] = make_float4(u[0], u[1], u[2], u[3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int k2 = 0; k2 < KMAX; ++k2) {
+                            if (k2 >= K) break;
+                            const int ej = pk[k2];
+                            const bool on = ej >= 0 && ej / Er == d;
+                            p.out.recv_topk_idx[n * K + k2] = on ? ej - lo : -1;
+                            p.out.recv_topk_weights[n * K + k2] = on ? wk[k2] : 0.0f;
+                        }
+                    }
+                }
+            }
+            const uint32_t *m = s_mask + e * kXWords;
+            int pos = s_excl[e] + __popc(m[warp] & below);
+            for (int w = 0; w < warp; ++w) pos += __popc(m[w]);
+            const int64_t g = static_cast<int64_t>(eoff[b]) + pos;
+            if (g < 0 || g >= p.rows_cap) {
+                set_error(p.dev.err, EP_ERR_CAPACITY);
+                continue;
+            }
+            p.out.expert_rows[g] = static_cast<int32_t>(n);
+        }
     }
 }
 

@@ -232,6 +232,58 @@ __device__ __forceinline__ void st_relaxed(unsigned long long *p, unsigned long 
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+// ---- decoupled look-back (Merrill & Garland 2016), shared by the scans
+// Descriptor word of one tile and column: {epoch:30 | flag:2 | value:32};
+// flag 1 = the tile's aggregate, 2 = the inclusive prefix through the tile.
+constexpr uint32_t kLookAggregate = 1u, kLookPrefix = 2u;
+constexpr int kLookBatch = 8;   // predecessors read per round trip
+
+__device__ __forceinline__ unsigned long long look_desc(uint32_t epoch, uint32_t flag, uint32_t value) {
+    return (static_cast<unsigned long long>(epoch) << 34) | (static_cast<unsigned long long>(flag) << 32) | value;
+}
+
+// Exclusive prefix of `tile` in one column: walks back over the predecessors'
+// descriptors (column entry c of tile t at desc[t * stride + c]), adding
+// aggregates until an inclusive prefix is found.  kLookBatch descriptors are
+// read per round trip; the walk stops at the first one not yet published in
+// this epoch and polls it again.  Bounded by timeout_ns from t_start: on
+// expiry it sets EP_ERR_TIMEOUT and returns what it has.
+__device__ __forceinline__ int lookback_excl(const unsigned long long *desc, int64_t stride, int c, int tile,
+                                             uint32_t epoch, uint64_t t_start, uint64_t timeout_ns, int32_t *err) {
+    int excl = 0;
+    int pred = tile - 1;
+    uint32_t spins = 0;
+    while (pred >= 0) {
+        unsigned long long v[kLookBatch];
+#pragma unroll
+        for (int q = 0; q < kLookBatch; ++q)
+            v[q] = pred - q >= 0 ? ld_relaxed(desc + static_cast<int64_t>(pred - q) * stride + c) : 0ull;
+        bool found = false, stall = false;
+#pragma unroll
+        for (int q = 0; q < kLookBatch; ++q) {
+            if (found || stall || pred < 0) continue;
+            const uint32_t ep_v = static_cast<uint32_t>(v[q] >> 34);
+            const uint32_t flag = static_cast<uint32_t>(v[q] >> 32) & 3u;
+            if (ep_v == epoch && flag != 0u) {
+                excl += static_cast<int>(static_cast<uint32_t>(v[q]));
+                if (flag == kLookPrefix) found = true;
+                --pred;
+            } else {
+                stall = true;
+            }
+        }
+        if (found) break;
+        if (stall && (++spins & 7u) == 0u) {
+            if (globaltimer_ns() - t_start > timeout_ns) {
+                set_error(err, EP_ERR_TIMEOUT);
+                break;
+            }
+            __nanosleep(64);
+        }
+    }
+    return excl;
+}
+
 // ---- mbarrier (shared::cta)
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

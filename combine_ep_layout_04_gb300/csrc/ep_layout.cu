@@ -38,11 +38,6 @@ constexpr int kTile = 256;
 constexpr int kWarps = kTile / 32;
 constexpr int kHistCap = 4096;             // shared-memory histogram bins
 constexpr unsigned kFull = 0xffffffffu;
-constexpr uint32_t kFlagAggregate = 1, kFlagPrefix = 2;
-
-__device__ __forceinline__ unsigned long long pack_desc(uint32_t epoch, uint32_t flag, uint32_t value) {
-    return (static_cast<unsigned long long>(epoch) << 34) | (static_cast<unsigned long long>(flag) << 32) | value;
-}
 
 // Exclusive scan of s[0, n) in place by the whole block (blockDim == kTile):
 // each thread scans a run of consecutive items, warps scan the run totals with
@@ -271,31 +266,11 @@ __global__ void __launch_bounds__(kTile) layout_kernel(const LayoutParams p) {
         unsigned long long *mine = p.dev.tile_desc + static_cast<int64_t>(tile) * R + d;
         int excl = 0;
         if (tile == 0) {
-            st_relaxed(mine, pack_desc(epoch, kFlagPrefix, static_cast<uint32_t>(agg)));
+            st_relaxed(mine, look_desc(epoch, kLookPrefix, static_cast<uint32_t>(agg)));
         } else {
-            st_relaxed(mine, pack_desc(epoch, kFlagAggregate, static_cast<uint32_t>(agg)));
-            int pred = tile - 1;
-            const uint64_t t_start = globaltimer_ns();
-            uint32_t spins = 0;
-            while (pred >= 0) {
-                const unsigned long long v = ld_relaxed(p.dev.tile_desc + static_cast<int64_t>(pred) * R + d);
-                const uint32_t ep_v = static_cast<uint32_t>(v >> 34);
-                const uint32_t flag = static_cast<uint32_t>(v >> 32) & 3u;
-                if (ep_v == epoch && flag != 0u) {
-                    excl += static_cast<int>(static_cast<uint32_t>(v));
-                    if (flag == kFlagPrefix) break;
-                    --pred;
-                    continue;
-                }
-                if ((++spins & 63u) == 0u) {
-                    if (globaltimer_ns() - t_start > kDefaultTimeoutNs) {
-                        set_error(p.dev.err, EP_ERR_TIMEOUT);
-                        break;
-                    }
-                    __nanosleep(64);
-                }
-            }
-            st_relaxed(mine, pack_desc(epoch, kFlagPrefix, static_cast<uint32_t>(excl + agg)));
+            st_relaxed(mine, look_desc(epoch, kLookAggregate, static_cast<uint32_t>(agg)));
+            excl = lookback_excl(p.dev.tile_desc, R, d, tile, epoch, globaltimer_ns(), kDefaultTimeoutNs, p.dev.err);
+            st_relaxed(mine, look_desc(epoch, kLookPrefix, static_cast<uint32_t>(excl + agg)));
         }
         s_excl[d] = excl;
         if (tile == p.tiles - 1) p.dev.col_prefix[R * R + d] = excl + agg;
