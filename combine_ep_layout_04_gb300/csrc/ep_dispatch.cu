@@ -72,7 +72,7 @@ namespace {
 constexpr int kThreads = 320;   // copy CTAs use warps 0-2; channel CTAs 0-9
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMetaSlots = 3;       // destination lists in flight (copy CTAs)
-constexpr int kDoneSlots = 16;      // chunks stored but not yet reported complete
+constexpr int kDoneSlots = 32;      // chunks stored but not yet reported complete
 constexpr int kPrefetchItems = 4;   // row loads in flight per copy CTA
 constexpr int kStoreLagItems = 2;   // items whose stores may still be in flight
 constexpr int kMaxPollRounds = 16;  // up to 512 slots examined per consumer step
@@ -86,18 +86,28 @@ constexpr int kNoticeLoads = 8;           // notice entries a poster lane keeps 
 // Shared words (u64) after rbase: abort flag; chunks complete (copy CTA) or
 // ring tail = retire point (channel CTA); poller stopped; ring base; dispatch
 // generation; messages expected on the channel; ring head; records logged;
-// chunk ids drawn (copy CTA); chunks stored in all, once known (copy CTA).
-// Then, in copy CTAs, the drawn chunk ids (a ring of kIdSlots ints).
+// chunk ids drawn (copy CTA); chunks stored in all, once known (copy CTA);
+// items loaded in all + 1, once known (copy CTA, vector-store path).
+// Then, in copy CTAs, the drawn chunk ids (a ring of kIdSlots ints) and, per
+// stage, the description of the item it holds (vector-store path).
 enum {
     kWAbort = 0, kWProgress = 1, kWStopped = 2, kWBase = 3, kWGen = 4, kWExpected = 5, kWHead = 6, kWLogged = 7,
-    kWIds = 8, kWCopyDone = 9
+    kWIds = 8, kWCopyDone = 9, kWItems = 10
 };
-constexpr int kNumWords = 10;
+constexpr int kNumWords = 11;
 constexpr int kIdSlots = 32;   // chunk ids a copy CTA has drawn but not yet retired
+constexpr int kStagesMax = 15;
+
+// Rows of at most kVecRowMax bytes leave shared memory by vector stores from
+// the copy CTA's store warps (warps kStoreWarp0..) instead of TMA bulk
+// stores: a bulk store costs about the same whatever its size, so for small
+// rows the TMA unit, not HBM, set the pace.
+constexpr int kVecRowMax = 4096;
+constexpr int kStoreWarp0 = 3;
 
 // Shared-memory carve, identical on host and device.
 struct SmemLayout {
-    int stage_off, meta_off, meta_slot_bytes, scratch_off, bar_off, total;
+    int stage_off, meta_off, meta_slot_bytes, scratch_off, info_off, bar_off, total;
     __host__ __device__ static int ring_off(int R) { return ((12 * R * R) + 127) / 128 * 128; }
     // poster ranges: per poster warp, 32 chunks x ceil(R/C) int2
     __host__ __device__ static int ranges_off(int R, int D) { return ring_off(R) + 16 * D + 16 * kLogStage; }
@@ -116,9 +126,12 @@ struct SmemLayout {
         meta_off = stage_area > channel ? stage_area : channel;
         meta_slot_bytes = ((32 * R + 33) + 3) / 4 * 16;   // dst[32*R] | pref[33]
         scratch_off = meta_off + meta_slot_bytes * kMetaSlots;
-        // scratch: rbase[R] ints, kNumWords u64 words, kIdSlots ints
-        bar_off = (scratch_off + ((R + 3) & ~3) * 4 + 8 * kNumWords + 4 * kIdSlots + 15) & ~15;
-        total = bar_off + 8 * (stages + 2 * kMetaSlots);
+        // scratch: rbase[R] ints, kNumWords u64 words, kIdSlots ints,
+        // kStagesMax item descriptions (int4)
+        info_off = (scratch_off + ((R + 3) & ~3) * 4 + 8 * kNumWords + 4 * kIdSlots + 15) & ~15;
+        bar_off = info_off + 16 * kStagesMax;
+        // barriers: stage_full[stages], meta_full[3], meta_free[3], stage_empty[stages]
+        total = bar_off + 8 * (2 * stages + 2 * kMetaSlots);
     }
 };
 
@@ -177,7 +190,7 @@ struct ItemCursor {
 };
 
 struct Bars {
-    uint64_t *stage_full, *meta_full, *meta_free;
+    uint64_t *stage_full, *meta_full, *meta_free, *stage_empty;
 };
 
 // ------------------------------------------------------------ copy CTA: copy
@@ -327,6 +340,180 @@ __device__ void copy_warp(const DispatchParams &p, uint8_t *smem, const SmemLayo
     // be reset between calls, which the last CTA does
     if (lane == 0) st_release_cta_shared(&words[kWCopyDone], ok ? static_cast<unsigned long long>(stored_chunks) + 1ull
                                                                 : 1ull);
+}
+
+// ------------------------------------------- copy CTA: small rows, loads
+// The vector-store path.  The copy warp only loads: per item it waits until
+// the item's stage is given back, writes the item's description (meta slot,
+// chunk number, tokens, last-of-chunk), and issues the TMA load.  It gives the
+// chunk to the notify warp once the store warps have given back every item
+// of the chunk (their mbarrier arrivals order their stores before it).
+__device__ void copy_warp_vec(const DispatchParams &p, uint8_t *smem, const SmemLayout &L, const Bars &bars,
+                              unsigned long long *words, int *ids, int4 *info) {
+    const int lane = threadIdx.x & 31;
+    const int S = p.stages;
+    const int64_t B = p.row_bytes;
+    int64_t n_loaded = 0, n_back = 0;
+    int chunks = 0, reported = 0;
+    int64_t last_item[kDoneSlots];   // last item of chunks loaded but not yet reported
+#pragma unroll
+    for (int i = 0; i < kDoneSlots; ++i) last_item[i] = 0;
+    bool ok = true;
+
+    unsigned int ahead = 0;
+    if (lane == 0) ahead = atomicAdd(p.dev.chunk_next, 1u);
+    int n_drawn = 0;
+    auto draw = [&]() -> int {   // warp-uniform
+        int k = -1;
+        if (lane == 0) {
+            k = ahead < static_cast<unsigned>(p.k1 - p.k0) ? p.k0 + static_cast<int>(ahead) : -1;
+            if (k >= 0) ahead = atomicAdd(p.dev.chunk_next, 1u);
+            ids[n_drawn % kIdSlots] = k;
+        }
+        k = __shfl_sync(kFull, k, 0);
+        ++n_drawn;
+        __syncwarp();
+        if (lane == 0) st_release_cta_shared(&words[kWIds], static_cast<unsigned long long>(n_drawn));
+        return k;
+    };
+    // take back the items the store warps have finished, in order; report the
+    // chunks whose every item is back.  Blocking: wait until item `until` is.
+    auto take_back = [&](int64_t until) {
+        while (n_back < n_loaded && ok) {
+            uint64_t *bar = &bars.stage_empty[n_back % S];
+            const uint32_t par = static_cast<uint32_t>(n_back / S) & 1u;
+            if (!__all_sync(kFull, mbar_test(bar, par))) {
+                if (n_back > until) break;
+                if (!warp_wait(bar, par, p)) {
+                    set_error(p.dev.err, EP_ERR_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+            }
+            ++n_back;
+        }
+        const int before = reported;
+        while (reported < chunks && last_item[reported % kDoneSlots] < n_back) ++reported;
+        if (reported != before) {
+            __syncwarp();
+            if (lane == 0) st_release_cta_shared(&words[kWProgress], static_cast<unsigned long long>(reported));
+        }
+    };
+
+    ItemCursor ld;
+    int ld_m = 0;
+    ld.set_chunk(p, draw());
+    while (ld.valid() && ok) {
+        if (n_loaded >= S) take_back(n_loaded - S);   // the stage's previous item
+        if (!ok) break;
+        fence_proxy_async_shared();   // the store warps' reads of the stage before the refill
+        int ta, tb, off, len;
+        ld.geometry(p, ta, tb, off, len);
+        const int st = static_cast<int>(n_loaded % S);
+        const int last = ld.q == ld.nitems - 1;
+        if (lane == 0) {
+            info[st] = make_int4(ld_m, ta, tb, last);
+            const uint32_t bytes = static_cast<uint32_t>((tb - ta) * len);
+            const uint8_t *src = p.x + (chunk_tok0(p, ld.k) + ta) * B + off;
+            mbar_arrive_expect_tx(&bars.stage_full[st], bytes);   // releases the description too
+            bulk_g2s(smem + L.stage_off + static_cast<int64_t>(st) * p.stage_bytes, src, bytes,
+                     &bars.stage_full[st]);
+        }
+        if (last) {
+            last_item[chunks % kDoneSlots] = n_loaded;
+            ++chunks;
+        }
+        ++n_loaded;
+        if (++ld.q >= ld.nitems) {
+            ++ld_m;
+            ld.set_chunk(p, draw());
+        }
+        take_back(-1);
+    }
+    __syncwarp();
+    if (lane == 0) st_release_cta_shared(&words[kWItems], static_cast<unsigned long long>(n_loaded) + 1ull);
+    if (ok) {
+        take_back(n_loaded - 1);
+    } else {
+        // abort: let every load already issued land before the CTA exits
+        for (int64_t j = n_back; j < n_loaded; ++j)
+            mbar_wait_bounded(&bars.stage_full[j % S], static_cast<uint32_t>(j / S) & 1u, nullptr, p.timeout_ns);
+        __syncwarp();
+    }
+    if (lane == 0) st_release_cta_shared(&words[kWCopyDone], ok ? static_cast<unsigned long long>(chunks) + 1ull
+                                                                : 1ull);
+}
+
+// ------------------------------------------ copy CTA: small rows, stores
+// Store warp w of the vector-store path takes, of every item, the (row,
+// destination) pairs w, w + store_warps, ...: the 32 lanes move the row from
+// the stage to its receive row with 16-byte loads and stores.  Then it gives
+// the stage back, and, after the last item of a chunk, the chunk's meta slot.
+__device__ void store_warp(const DispatchParams &p, uint8_t *smem, const SmemLayout &L, const Bars &bars,
+                           unsigned long long *words, const int4 *info, int w) {
+    const int lane = threadIdx.x & 31;
+    const int S = p.stages;
+    const int64_t B = p.row_bytes;
+    const int nseg = static_cast<int>(B / 16);
+    int cur_m = -1;
+    for (int64_t i = 0;; ++i) {
+        const int st = static_cast<int>(i % S);
+        const uint32_t par = static_cast<uint32_t>(i / S) & 1u;
+        // item i, once loaded, or the end
+        const uint64_t t0 = globaltimer_ns();
+        bool have = false, end = false;
+        unsigned nap = 32;
+        while (true) {
+            have = __all_sync(kFull, mbar_test(&bars.stage_full[st], par));
+            if (have) break;
+            const unsigned long long items = ld_acquire_cta_shared(&words[kWItems]);
+            if (items != 0ull && static_cast<unsigned long long>(i) + 1ull >= items) {
+                end = true;
+                break;
+            }
+            bool give_up = read_error(p.dev.err) != 0 || globaltimer_ns() - t0 > p.timeout_ns;
+            if (__any_sync(kFull, give_up)) {
+                if (read_error(p.dev.err) == 0) set_error(p.dev.err, EP_ERR_TIMEOUT);
+                end = true;
+                break;
+            }
+            __nanosleep(nap);
+            nap = min(nap * 2u, 256u);
+        }
+        if (end) return;
+        const int4 it = info[st];   // m, ta, tb, last
+        const int slot = it.x % kMetaSlots;
+        if (it.x != cur_m) {
+            if (!warp_wait(&bars.meta_full[slot], static_cast<uint32_t>(it.x / kMetaSlots) & 1u, p)) {
+                set_error(p.dev.err, EP_ERR_TIMEOUT);
+                return;
+            }
+            cur_m = it.x;
+        }
+        const MetaSlot ms(smem + L.meta_off + static_cast<int64_t>(slot) * L.meta_slot_bytes, p.R);
+        const uint8_t *stage_base = smem + L.stage_off + static_cast<int64_t>(st) * p.stage_bytes;
+        const int ta = it.y, tb = it.z;
+        const int pb = ms.pref[ta], pe = ms.pref[tb];
+        int tl = ta;
+        for (int pi = pb + w; pi < pe; pi += p.store_warps) {
+            while (ms.pref[tl + 1] <= pi) ++tl;
+            const int row = ms.dst[tl * p.R + (pi - ms.pref[tl])];
+            const uint8_t *src = stage_base + static_cast<int64_t>(tl - ta) * B;
+            uint8_t *dst = p.recv + static_cast<int64_t>(row) * B;
+            uint4 v[kVecRowMax / 16 / 32];
+#pragma unroll
+            for (int q = 0; q < kVecRowMax / 16 / 32; ++q)
+                if (lane + 32 * q < nseg) v[q] = ld_shared_v4(src + 16 * (lane + 32 * q));
+#pragma unroll
+            for (int q = 0; q < kVecRowMax / 16 / 32; ++q)
+                if (lane + 32 * q < nseg) *reinterpret_cast<uint4 *>(dst + 16 * (lane + 32 * q)) = v[q];
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&bars.stage_empty[st]);
+            if (it.w) mbar_arrive(&bars.meta_free[slot]);
+        }
+    }
 }
 
 // ------------------------------------------------------------ copy CTA: meta
@@ -867,6 +1054,8 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
     bars.stage_full = b;
     bars.meta_full = b + p.stages;
     bars.meta_free = bars.meta_full + kMetaSlots;
+    bars.stage_empty = bars.meta_free + kMetaSlots;
+    int4 *item_info = reinterpret_cast<int4 *>(smem + L.info_off);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool channel_cta = static_cast<int>(blockIdx.x) < p.C;
 
@@ -874,10 +1063,14 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
     // so that either all of them run or none does.
     if (warp == 0 && lane == 0) {
         if (!channel_cta) {
-            for (int i = 0; i < p.stages; ++i) mbar_init(&bars.stage_full[i], 1);
+            const int store_warps = p.vec_store ? p.store_warps : 1;
+            for (int i = 0; i < p.stages; ++i) {
+                mbar_init(&bars.stage_full[i], 1);
+                mbar_init(&bars.stage_empty[i], store_warps);
+            }
             for (int i = 0; i < kMetaSlots; ++i) {
                 mbar_init(&bars.meta_full[i], 1);
-                mbar_init(&bars.meta_free[i], 1);
+                mbar_init(&bars.meta_free[i], store_warps);
             }
             mbar_fence_init();
         }
@@ -957,8 +1150,12 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
                     consumer_log(p, c, expected, words, stage);
             }
         } else {
-            if (warp == 0)
+            if (warp == 0 && p.vec_store)
+                copy_warp_vec(p, smem, L, bars, words, ids, item_info);
+            else if (warp == 0)
                 copy_warp(p, smem, L, bars, words, ids);
+            else if (warp >= kStoreWarp0 && p.vec_store)
+                store_warp(p, smem, L, bars, words, item_info, warp - kStoreWarp0);
             else if (warp == 1)
                 meta_warp(p, smem, L, bars, rbase, words, ids);
             else if (warp == 2)
@@ -1012,7 +1209,7 @@ ep_status plan_dispatch(ep_ctx *h) {
         return EP_ERR_CUDA;
     const int reserve = 1024;   // static + alignment slack
     int stages = 0;
-    for (int s = 15; s >= 3; --s) {
+    for (int s = kStagesMax; s >= 3; --s) {
         SmemLayout L(R, C, h->cfg.ring_depth, stage_bytes, s);
         if (L.total + reserve <= max_smem) {
             stages = s;
@@ -1022,6 +1219,7 @@ ep_status plan_dispatch(ep_ctx *h) {
     if (stages == 0) return EP_ERR_INVALID_ARG;
     SmemLayout L(R, C, h->cfg.ring_depth, stage_bytes, stages);
     h->rows_per_item = rows_per_item;
+    h->vec_store = (pieces == 1 && B <= kVecRowMax) ? 1 : 0;
     h->pieces = pieces;
     h->piece_bytes = piece_bytes;
     h->stage_bytes = stage_bytes;
@@ -1089,6 +1287,8 @@ ep_status launch_dispatch(ep_ctx *h, const void *x, const ep_layout_out *lay, vo
     p.meta_slots = h->meta_slots;
     p.slot_vec = (p.R % 4 == 0 && reinterpret_cast<uintptr_t>(lay->token_slot) % 16 == 0) ? 1 : 0;
     p.lg_depth = __builtin_ctz(static_cast<unsigned>(p.D));
+    p.vec_store = h->vec_store;
+    p.store_warps = kThreads / 32 - kStoreWarp0;
     void *args[] = {&p};
     const cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(dispatch_kernel),
                                                       dim3(h->disp_grid), dim3(kThreads), args, h->disp_smem, st);

@@ -91,6 +91,8 @@ struct DispatchParams {
     int stages, prefetch, meta_slots;
     int store_lag;       // items whose bulk stores may be in flight
     int slot_vec;        // 1: token_slot rows are 16-byte aligned (int4 loads)
+    int vec_store;       // 1: rows leave shared memory by the store warps' vector stores
+    int store_warps;     // store warps per copy CTA on that path
     int lg_depth;        // log2(D)
 };
 
@@ -128,6 +130,7 @@ struct ep_ctx {
     int stage_bytes, stages, prefetch, meta_slots, store_lag;
     int rows_per_item, pieces, piece_bytes;
     int chunks_per_rank, nchunks, chunk_tokens;
+    int vec_store;
     int64_t log_cap;
     // combine geometry
     int comb_grid, comb_threads;
@@ -382,6 +385,18 @@ __device__ __forceinline__ void bulk_wait_n(int n) {
 }
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// generic-proxy accesses to shared memory before later async-proxy (TMA) ones
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.shared::cta.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_u32_(p))
+                 : "memory");
+    return v;
 }
 
 #endif  // __CUDACC__
