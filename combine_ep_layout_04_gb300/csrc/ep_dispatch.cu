@@ -18,9 +18,9 @@
 // How: one persistent cooperative kernel, one CTA per SM, in two kinds.
 //
 // Copy CTAs (all but the first C) move the rows.  Chunks of 4 to 32 tokens of
-// one source rank (about four per copy CTA at most) are drawn from a
+// one source rank (about four per copy CTA at least) are drawn from a
 // device-wide counter (so faster SMs take more);
-// three warps hand each chunk on through mbarriers and shared counters:
+// their warps hand each chunk on through mbarriers and shared counters:
 //   copy    1-D TMA bulk loads of token rows (a run of whole rows when they
 //           are small, a piece of one row when it is large) into a ring of
 //           shared-memory stages, then one TMA bulk store per (row,
@@ -29,6 +29,11 @@
 //           loads; all 32 lanes issue stores, each tracking its own bulk
 //           groups, so a stage is recycled only once every lane's stores from
 //           it have completed.
+//   store   (rows of at most 4 KB only) seven warps take the stores over:
+//           the copy warp only loads, and the store warps move each (row,
+//           destination) pair from the stage with 16-byte vector stores --
+//           a TMA bulk store costs about the same whatever its size, so for
+//           small rows TMA, not HBM, would set the pace.
 //   meta    reads the chunk's token_slot rows; builds each token's
 //           destination-row list (for the copy warp) and writes the chunk's
 //           notice -- the first and last window slot it covers per
@@ -37,13 +42,15 @@
 //           chunk's ready flag (tagged with the dispatch's generation).
 //
 // Channel CTAs (the first C) each own ring c = blockIdx.x:
-//   poster  walks every chunk in order, waits for its ready flag, and turns
-//           its notice into the messages of ring c that the chunk completes:
-//           a message of G rows is complete in the chunk that holds its last
-//           row, since all earlier rows of the pair are in earlier chunks.
-//           It posts them in batches of up to `batch` commands: one atomicAdd
-//           on head per batch, a wait while the ring would hold more than
-//           max_inflight commands, then the slot stores.
+//   poster  (eight warps) takes groups of 32 chunks in turn, waits for their
+//           ready flags, and turns their notices into the messages of ring c
+//           that the chunks complete: a message of G rows is complete in the
+//           chunk that holds its last row, since all earlier rows of the pair
+//           are in earlier chunks.  It posts them in batches of up to `batch`
+//           commands: one atomicAdd on head per batch, a wait while the ring
+//           would hold more than max_inflight commands, then the slot stores;
+//           then it adds the group's messages to the destinations' arrival
+//           signals.
 //   poller  examines every slot that can be outstanding (drain_batch = 32 per
 //           warp-wide load), takes the longest run of published slots, stages
 //           the records for the logger and moves the tail (the retire point)

@@ -231,7 +231,9 @@ ep_status ep_layout(ep_handle h, const int32_t *topk_idx, const ep_layout_out *o
  * control; s4.2 channels).  Consumer warps on the device retire each ring into
  * its log (ep_cmd_log) and advance its tail; the kernel ends when every ring
  * is drained ([UCCL-EP] s3.1 Drain).  One persistent cooperative kernel; rows
- * move by TMA bulk copies through shared memory, each source row read once.
+ * move through shared memory, each source row read once: TMA bulk loads, then
+ * TMA bulk stores (rows over 4 KB) or vector stores from seven store warps
+ * (rows of at most 4 KB).
  *  x:      device bf16 [T, H].
  *  layout: outputs of ep_layout for this routing (read on the device).
  *  recv:   device bf16 [recv_capacity_rows, H]; rows [0, N) are written.
