@@ -723,184 +723,189 @@ __device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long
     uint64_t err_checked = globaltimer_ns();
     for (int grp = w; grp < ngroups && !failed; grp += kPosterWarps) {
         const int k = p.k0 + grp * 32 + lane;
-        // The group's chunks complete within a few microseconds of each other
-        // (they are drawn in order): wait for all of them, polling device
-        // memory with a back-off, before posting -- so that while posting
-        // the warp touches shared memory only and answers the ring at once.
-        {
-            bool rdy = k >= p.k1;
-            const uint64_t tw = globaltimer_ns();
-            unsigned nap = 256;
-            while (!__all_sync(kFull, rdy)) {
-                if (!rdy) rdy = ld_acquire_u32(p.dev.ready + k) == tag;
-                if (__all_sync(kFull, rdy)) break;
-                bool give_up = false;
-                if (!rdy && (read_error(p.dev.err) != 0 || globaltimer_ns() - tw > p.timeout_ns)) give_up = true;
-                if (__any_sync(kFull, give_up)) {
-                    if (read_error(p.dev.err) == 0) set_error(p.dev.err, EP_ERR_TIMEOUT);
-                    failed = true;
-                    break;
-                }
-                __nanosleep(nap);
-                nap = min(nap * 2u, 4096u);
-            }
-            if (failed) break;
-        }
-        // this lane's chunk: messages [gb, ge) per destination of ring c
-        int total = 0;
-        {
-            bool bad = false;
-            if (k < p.k1) {
-                const int s = k / p.chunks_per_rank;
-                const int32_t *nt = p.dev.notice + static_cast<int64_t>(k) * 2 * R;
-                // kNoticeLoads destinations' notices in flight at once
-                int2 lhs[kNoticeLoads];
-                for (int i = 0; i < nd; ++i) {
-                    const int d = c + i * C;
-                    if (i % kNoticeLoads == 0) {
-#pragma unroll
-                        for (int b = 0; b < kNoticeLoads; ++b)
-                            lhs[b] = i + b < nd ? __ldcg(reinterpret_cast<const int2 *>(nt + 2 * (d + b * C)))
-                                                : make_int2(-1, -1);
-                    }
-                    int2 lh = lhs[0];
-#pragma unroll
-                    for (int b = 1; b < kNoticeLoads; ++b)
-                        if (i % kNoticeLoads == b) lh = lhs[b];
-                    int gb = 0, ge = 0;
-                    if (lh.y >= 0) {
-                        const int cnt = pt.cnt[s * R + d], r0 = pt.recv0[s * R + d];
-                        const int jlo = lh.x - r0, jhi = lh.y - r0;
-                        if (jlo < 0 || jhi < jlo || jhi >= cnt) {
-                            bad = true;
-                        } else {
-                            gb = jlo / G;
-                            ge = max(gb, (jhi == cnt - 1) ? (cnt - 1) / G + 1 : (jhi + 1) / G);
-                        }
-                    }
-                    ranges[lane * ndmax + i] = make_int2(gb, ge);
-                    total += ge - gb;
-                }
-            }
-            if (bad) {
-                set_error(p.dev.err, EP_ERR_INVALID_ARG);
-                total = 0;
-            }
-            __syncwarp();
-        }
-        // Post the group's commands.  Each lane lists its own chunk's next
-        // commands (at most kListPerLane) into the warp's list, packed the way
-        // a slot holds them; the warp then posts the list, 32 (whole batches)
-        // a round, one command per lane.  A batch may span chunks.
-        int left = total;            // this lane's commands not yet listed
-        int ci = 0, cm = 0;          // cursor: destination index, message past gb
-        const int s_lane = k < p.k1 ? k / p.chunks_per_rank : 0;
-        while (!failed) {
-            const int take = min(left, kListPerLane);
-            int incl = take;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(kFull, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const int ltot = __shfl_sync(kFull, incl, 31);
-            if (ltot == 0) break;
-            for (int q = 0, at = incl - take; q < take; ++q, ++at) {
-                int2 g = ranges[lane * ndmax + ci];
-                while (cm >= g.y - g.x) {
-                    ++ci;
-                    cm = 0;
-                    g = ranges[lane * ndmax + ci];
-                }
-                const int d = c + ci * C, pi = s_lane * R + d;
-                const int j0 = (g.x + cm) * G;
-                const int rows = min(G, pt.cnt[pi] - j0);
-                st_shared_v2(list + 2 * at,
-                             (static_cast<unsigned long long>(d) << 42) | (static_cast<unsigned long long>(rows) << 31) |
-                                 static_cast<unsigned long long>(pt.send0[pi] + j0),
-                             static_cast<unsigned long long>(pt.recv0[pi] + j0));
-                ++cm;
-            }
-            left -= take;
-            __syncwarp();
-            for (int r0 = 0; r0 < ltot && !failed; r0 += rs) {
-                const int nround = min(rs, ltot - r0);
-                const bool mine = lane < nround;
-                unsigned long long w0 = 0ull, w1 = 0ull;
-                if (mine) {
-                    const ulonglong2 v = ld_shared_v2(list + 2 * (r0 + lane));
-                    w0 = v.x;
-                    w1 = v.y;
-                }
-                // batch leaders reserve; every lane learns its batch's base
-                const int n = mine ? min(p.batch, nround - leader) : 0;
-                unsigned long long base = 0ull;
-                if (mine && lane == leader) base = atomicAdd(head, static_cast<unsigned long long>(n));
-                base = __shfl_sync(kFull, base, leader);
-                const unsigned long long idx = base + static_cast<unsigned long long>(lane - leader);
-                bool pending = mine;
-                uint64_t t0 = globaltimer_ns();
-                unsigned sleep = 32;
-                unsigned long long stalls = 0;
+        // Post the group's chunks as they become ready: wait until at least
+        // one pending chunk's flag is set (polling device memory with a
+        // back-off), post every chunk found ready, and come back for the
+        // rest.  While posting, the warp touches shared memory only and
+        // answers the ring at once.
+        bool pending = k < p.k1;          // this lane's chunk is not yet posted
+        const uint64_t tw = globaltimer_ns();
+        while (__any_sync(kFull, pending) && !failed) {
+            bool take_now = false;
+            {
+                unsigned nap = 128;
                 while (true) {
-                    if (pending) {
-                        const unsigned long long tail = ld_acquire_cta_shared(&words[kWProgress]);
-                        if (base + n - tail <= limit) {
-                            const unsigned long long lt = lap_tag(idx, p.lg_depth);
-                            st_shared_v2(ring + 2 * (idx & dmask), w0 | lt, w1 | lt);
-                            if (lane == leader) {
-                                st.batches += 1;
-                                st.max_batch = max(st.max_batch, static_cast<unsigned>(n));
-                                st.max_inflight = max(st.max_inflight, static_cast<unsigned>(base + n - tail));
-                                st.stalls += stalls;
-                            }
-                            pending = false;
-                        } else {
-                            ++stalls;
-                        }
-                    }
-                    if (!__any_sync(kFull, pending)) break;
-                    // waiting touches shared memory only; the device error word
-                    // (an L2 round trip) is read every few tens of microseconds
-                    bool give_up = false;
-                    if (pending) {
-                        const uint64_t now = globaltimer_ns();
-                        if (now - t0 > p.timeout_ns) {
-                            set_error(p.dev.err, EP_ERR_TIMEOUT);
-                            give_up = true;
-                        } else if (now - err_checked > kErrCheckNs) {
-                            err_checked = now;
-                            give_up = read_error(p.dev.err) != 0;
-                        }
-                    }
+                    if (pending && !take_now) take_now = ld_acquire_u32(p.dev.ready + k) == tag;
+                    if (__any_sync(kFull, take_now)) break;
+                    const bool give_up =
+                        pending && (read_error(p.dev.err) != 0 || globaltimer_ns() - tw > p.timeout_ns);
                     if (__any_sync(kFull, give_up)) {
+                        if (read_error(p.dev.err) == 0) set_error(p.dev.err, EP_ERR_TIMEOUT);
                         failed = true;
                         break;
                     }
-                    __nanosleep(sleep);
-                    sleep = min(sleep * 2u, 64u);
+                    __nanosleep(nap);
+                    nap = min(nap * 2u, 2048u);
                 }
+                if (failed) break;
             }
-            __syncwarp();
-        }
-        // arrival signals: the group's messages to each destination have
-        // landed (their chunks' ready flags were acquired above) and are now
-        // posted -- one fence per group, then one add per destination
-        if (!failed) {
-            __syncwarp();
-            if (lane == 0) fence_acq_rel_gpu();
-            for (int i = 0; i < nd; ++i) {
-                int m = 0;
-                if (k < p.k1) {
-                    const int2 g = ranges[lane * ndmax + i];
-                    m = g.y - g.x;
-                }
+            pending = pending && !take_now;
+            // this lane's chunk: messages [gb, ge) per destination of ring c
+            int total = 0;
+            {
+                bool bad = false;
+                if (take_now) {
+                    const int s = k / p.chunks_per_rank;
+                    const int32_t *nt = p.dev.notice + static_cast<int64_t>(k) * 2 * R;
+                    // kNoticeLoads destinations' notices in flight at once
+                    int2 lhs[kNoticeLoads];
+                    for (int i = 0; i < nd; ++i) {
+                        const int d = c + i * C;
+                        if (i % kNoticeLoads == 0) {
 #pragma unroll
-                for (int o = 16; o; o >>= 1) m += __shfl_xor_sync(kFull, m, o);
-                if (lane == 0 && m > 0) red_add_relaxed(p.dev.signal + c + i * C, static_cast<unsigned long long>(m));
+                            for (int b = 0; b < kNoticeLoads; ++b)
+                                lhs[b] = i + b < nd ? __ldcg(reinterpret_cast<const int2 *>(nt + 2 * (d + b * C)))
+                                                    : make_int2(-1, -1);
+                        }
+                        int2 lh = lhs[0];
+#pragma unroll
+                        for (int b = 1; b < kNoticeLoads; ++b)
+                            if (i % kNoticeLoads == b) lh = lhs[b];
+                        int gb = 0, ge = 0;
+                        if (lh.y >= 0) {
+                            const int cnt = pt.cnt[s * R + d], r0 = pt.recv0[s * R + d];
+                            const int jlo = lh.x - r0, jhi = lh.y - r0;
+                            if (jlo < 0 || jhi < jlo || jhi >= cnt) {
+                                bad = true;
+                            } else {
+                                gb = jlo / G;
+                                ge = max(gb, (jhi == cnt - 1) ? (cnt - 1) / G + 1 : (jhi + 1) / G);
+                            }
+                        }
+                        ranges[lane * ndmax + i] = make_int2(gb, ge);
+                        total += ge - gb;
+                    }
+                }
+                if (bad) {
+                    set_error(p.dev.err, EP_ERR_INVALID_ARG);
+                    total = 0;
+                }
+                __syncwarp();
             }
+            // Post the group's commands.  Each lane lists its own chunk's next
+            // commands (at most kListPerLane) into the warp's list, packed the way
+            // a slot holds them; the warp then posts the list, 32 (whole batches)
+            // a round, one command per lane.  A batch may span chunks.
+            int left = total;            // this lane's commands not yet listed
+            int ci = 0, cm = 0;          // cursor: destination index, message past gb
+            const int s_lane = take_now ? k / p.chunks_per_rank : 0;
+            while (!failed) {
+                const int take = min(left, kListPerLane);
+                int incl = take;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(kFull, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const int ltot = __shfl_sync(kFull, incl, 31);
+                if (ltot == 0) break;
+                for (int q = 0, at = incl - take; q < take; ++q, ++at) {
+                    int2 g = ranges[lane * ndmax + ci];
+                    while (cm >= g.y - g.x) {
+                        ++ci;
+                        cm = 0;
+                        g = ranges[lane * ndmax + ci];
+                    }
+                    const int d = c + ci * C, pi = s_lane * R + d;
+                    const int j0 = (g.x + cm) * G;
+                    const int rows = min(G, pt.cnt[pi] - j0);
+                    st_shared_v2(list + 2 * at,
+                                 (static_cast<unsigned long long>(d) << 42) | (static_cast<unsigned long long>(rows) << 31) |
+                                     static_cast<unsigned long long>(pt.send0[pi] + j0),
+                                 static_cast<unsigned long long>(pt.recv0[pi] + j0));
+                    ++cm;
+                }
+                left -= take;
+                __syncwarp();
+                for (int r0 = 0; r0 < ltot && !failed; r0 += rs) {
+                    const int nround = min(rs, ltot - r0);
+                    const bool mine = lane < nround;
+                    unsigned long long w0 = 0ull, w1 = 0ull;
+                    if (mine) {
+                        const ulonglong2 v = ld_shared_v2(list + 2 * (r0 + lane));
+                        w0 = v.x;
+                        w1 = v.y;
+                    }
+                    // batch leaders reserve; every lane learns its batch's base
+                    const int n = mine ? min(p.batch, nround - leader) : 0;
+                    unsigned long long base = 0ull;
+                    if (mine && lane == leader) base = atomicAdd(head, static_cast<unsigned long long>(n));
+                    base = __shfl_sync(kFull, base, leader);
+                    const unsigned long long idx = base + static_cast<unsigned long long>(lane - leader);
+                    bool pending = mine;
+                    uint64_t t0 = globaltimer_ns();
+                    unsigned sleep = 32;
+                    unsigned long long stalls = 0;
+                    while (true) {
+                        if (pending) {
+                            const unsigned long long tail = ld_acquire_cta_shared(&words[kWProgress]);
+                            if (base + n - tail <= limit) {
+                                const unsigned long long lt = lap_tag(idx, p.lg_depth);
+                                st_shared_v2(ring + 2 * (idx & dmask), w0 | lt, w1 | lt);
+                                if (lane == leader) {
+                                    st.batches += 1;
+                                    st.max_batch = max(st.max_batch, static_cast<unsigned>(n));
+                                    st.max_inflight = max(st.max_inflight, static_cast<unsigned>(base + n - tail));
+                                    st.stalls += stalls;
+                                }
+                                pending = false;
+                            } else {
+                                ++stalls;
+                            }
+                        }
+                        if (!__any_sync(kFull, pending)) break;
+                        // waiting touches shared memory only; the device error word
+                        // (an L2 round trip) is read every few tens of microseconds
+                        bool give_up = false;
+                        if (pending) {
+                            const uint64_t now = globaltimer_ns();
+                            if (now - t0 > p.timeout_ns) {
+                                set_error(p.dev.err, EP_ERR_TIMEOUT);
+                                give_up = true;
+                            } else if (now - err_checked > kErrCheckNs) {
+                                err_checked = now;
+                                give_up = read_error(p.dev.err) != 0;
+                            }
+                        }
+                        if (__any_sync(kFull, give_up)) {
+                            failed = true;
+                            break;
+                        }
+                        __nanosleep(sleep);
+                        sleep = min(sleep * 2u, 64u);
+                    }
+                }
+                __syncwarp();
+            }
+            // arrival signals: the pass's messages to each destination have
+            // landed (their chunks' ready flags were acquired above) and are now
+            // posted -- one fence per pass, then one add per destination
+            if (!failed) {
+                __syncwarp();
+                if (lane == 0) fence_acq_rel_gpu();
+                for (int i = 0; i < nd; ++i) {
+                    int m = 0;
+                    if (take_now) {
+                        const int2 g = ranges[lane * ndmax + i];
+                        m = g.y - g.x;
+                    }
+#pragma unroll
+                    for (int o = 16; o; o >>= 1) m += __shfl_xor_sync(kFull, m, o);
+                    if (lane == 0 && m > 0) red_add_relaxed(p.dev.signal + c + i * C, static_cast<unsigned long long>(m));
+                }
+            }
+            __syncwarp();
         }
-        __syncwarp();
     }
     // statistics: one reduction per warp
     unsigned long long b = st.batches, sp = st.stalls;
