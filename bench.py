@@ -8,6 +8,12 @@ intervals on the launching stream.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload ht]
   python bench.py --impl reference ...   # the CPU oracle on the host, same metric
+  python bench.py --sweep msg            # dispatch bandwidth against row and message size
+  python bench.py --overlap              # layer pieces: sequential against pipelined
+  python bench.py --tokens-per-rank 256  # a smaller case of a workload (profiler captures)
+
+Beside the step, the JSON line carries `next_rows.expert_layout`: ep_expert_layout
+timed on its own after the timed region (it is not part of the step).
 
 Multi-GPU: the path does not shard across GPUs here (each simulated EP group
 lives in one GPU's memory), so N GPUs run N independent replicas; `value` is
