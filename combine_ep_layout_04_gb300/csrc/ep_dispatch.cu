@@ -76,7 +76,7 @@
 namespace ep {
 namespace {
 
-constexpr int kThreads = 320;   // copy CTAs use warps 0-2; channel CTAs 0-9
+constexpr int kThreads = 320;   // channel CTAs use all ten warps; copy CTAs three, or ten for small rows
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMetaSlots = 3;       // destination lists in flight (copy CTAs)
 constexpr int kDoneSlots = 32;      // chunks stored but not yet reported complete
@@ -685,17 +685,17 @@ struct PairTables {
 };
 
 // The posters of ring c.  Poster warp w takes chunk groups w, w + kPosterWarps,
-// ... of 32 chunks.  For a group it waits until every chunk is ready, then
-// lane i loads chunk 32 * group + i's notice for each destination of ring c
-// (one round trip for the group) and derives the messages the chunk
-// completes on ring c: those of pair (s, d) whose last row lies in the
-// chunk's rows [jlo, jhi] of the pair -- all earlier rows of the pair are in
-// earlier chunks.  The ranges go to shared memory.  Then, in passes, every
-// lane writes its chunk's next commands (packed as a slot holds them) into
-// the warp's list -- a walk along its own ranges, no search -- and the warp
-// posts the list one command per lane, 32 a round: the first lane of each
-// batch of up to `batch` lanes reserves the batch's slots with one atomicAdd
-// on head, and each lane stores its slot as soon as
+// ... of 32 chunks, lane i holding chunk 32 * group + i.  It polls the
+// group's ready flags and takes, pass by pass, the chunks found ready: each
+// such lane loads its chunk's notice for every destination of ring c (one
+// round trip) and derives the messages the chunk completes on ring c: those
+// of pair (s, d) whose last row lies in the chunk's rows [jlo, jhi] of the
+// pair -- all earlier rows of the pair are in earlier chunks.  The ranges go
+// to shared memory.  Then every lane writes its chunk's next commands (packed
+// as a slot holds them) into the warp's list -- a walk along its own ranges,
+// no search -- and the warp posts the list one command per lane, 32 a round:
+// the first lane of each batch of up to `batch` lanes reserves the batch's
+// slots with one atomicAdd on head, and each lane stores its slot as soon as
 // base + n - tail <= max_inflight (tail is the poller's retire point, in
 // shared memory).
 constexpr int kPosterWarps = 8;
