@@ -67,16 +67,22 @@ def read_peaks():
 
 
 def kernel_src_sha(kernel: str):
-    """First 16 hex digits of sha256 over the kernel's source file followed by
-    the shared device header: a counter taken on other source does not apply."""
+    """First 16 hex digits of sha256 over the code of the kernel's source file
+    followed by the shared device header, comments and whitespace removed: a
+    counter taken on other code does not apply, one taken before a comment
+    changed still does."""
     import hashlib
+    import re
     csrc = os.path.join(ROOT, "combine_ep_layout_04_gb300", "csrc")
     files = [os.path.join(csrc, f"ep_{kernel}.cu"), os.path.join(csrc, "ep_internal.cuh")]
     if not all(os.path.exists(f) for f in files):
         return None
     h = hashlib.sha256()
     for f in files:
-        h.update(open(f, "rb").read())
+        text = open(f, encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
