@@ -50,7 +50,15 @@ struct ExpertParams {
     int R, E, K, Er;
     int tiles;
     int vec4;              // K % 4 == 0 and the row outputs are 16-byte aligned
+    int vec8;              // K % 8 == 0 and the row outputs are 32-byte aligned
 };
+
+// One 32-byte store (st.global.v8.b32); p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&v)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]),
+                 "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
 
 template <int KMAX>
 __global__ void __launch_bounds__(kXTile) expert_layout_kernel(const ExpertParams p) {
@@ -168,7 +176,25 @@ __global__ void __launch_bounds__(kXTile) expert_layout_kernel(const ExpertParam
                 } else {
                     p.out.recv_src_token[n] = static_cast<int32_t>(t);
                     const int lo = d * Er;
-                    if (p.vec4) {
+                    if (p.vec8) {
+                        // whole 32-byte sectors: one store per eight picks
+                        int32_t *ri = p.out.recv_topk_idx + n * K;
+                        float *rw = p.out.recv_topk_weights + n * K;
+#pragma unroll
+                        for (int k8 = 0; k8 < KMAX; k8 += 8) {
+                            if (k8 >= K) break;
+                            uint32_t v[8], u[8];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const int ej = pk[k8 + j];
+                                const bool on = ej >= 0 && ej / Er == d;
+                                v[j] = static_cast<uint32_t>(on ? ej - lo : -1);
+                                u[j] = __float_as_uint(on ? wk[k8 + j] : 0.0f);
+                            }
+                            st_global_v8(ri + k8, v);
+                            st_global_v8(rw + k8, u);
+                        }
+                    } else if (p.vec4) {
                         int4 *ri = reinterpret_cast<int4 *>(p.out.recv_topk_idx + n * K);
                         float4 *rw = reinterpret_cast<float4 *>(p.out.recv_topk_weights + n * K);
 #pragma unroll
@@ -255,6 +281,7 @@ ep_status launch_expert_layout(ep_ctx *h, const int32_t *topk_idx, const float *
     const uintptr_t a = reinterpret_cast<uintptr_t>(out->recv_topk_idx) |
                         reinterpret_cast<uintptr_t>(out->recv_topk_weights);
     p.vec4 = (p.K % 4 == 0 && a % 16 == 0) ? 1 : 0;
+    p.vec8 = (p.K % 8 == 0 && a % 32 == 0) ? 1 : 0;
     const size_t smem = expert_smem_bytes(p.E);
     if (p.K <= 8)
         expert_layout_kernel<8><<<h->xtiles, kXTile, smem, st>>>(p);
