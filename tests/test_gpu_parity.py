@@ -122,6 +122,9 @@ def _w(**kw):
     dict(num_ranks=64, tokens_per_rank=40, hidden=64, num_experts=128, topk=8),  # the most ranks
     dict(num_ranks=33, tokens_per_rank=9, hidden=32, num_experts=66, topk=5),    # two column groups
     dict(num_ranks=4, tokens_per_rank=300, hidden=128, num_experts=64, topk=32),  # the largest top-k
+    dict(num_ranks=64, tokens_per_rank=24, hidden=2048, num_experts=256, topk=8),  # 4 KB rows, 64 ranks
+    dict(num_ranks=16, tokens_per_rank=1, hidden=1024, num_experts=32, topk=4),    # one token per rank
+    dict(num_ranks=8, tokens_per_rank=97, hidden=2056, num_experts=32, topk=6),    # 4112-byte rows: TMA path
 ])
 def test_edge_shapes(kw):
     run_and_check(_w(**kw))
@@ -130,7 +133,8 @@ def test_edge_shapes(kw):
 @pytest.mark.parametrize("opts", [
     dict(rows_per_msg=1), dict(rows_per_msg=3), dict(rows_per_msg=64), dict(batch=1), dict(channels=1),
     dict(channels=3), dict(ring_depth=16, max_inflight=8), dict(ring_depth=64, max_inflight=64, batch=5),
-    dict(drain_batch=64),
+    dict(drain_batch=64), dict(ring_depth=8192, max_inflight=8192), dict(rows_per_msg=2047),
+    dict(drain_batch=512, max_inflight=512),
 ])
 def test_ring_options(opts):
     w = _w(num_ranks=8, tokens_per_rank=100, hidden=512, num_experts=32, topk=4)
