@@ -8,12 +8,12 @@
 //   per expert e: the receive rows of its picks in token order, placed at
 //   expert_off[e] + j, and the count of its picks.
 //
-// How: one CTA per tile of 128 tokens (one token per thread), tiles handed
-// out in launch order by a ticket counter, so a tile's predecessors are
-// already running.  Per tile:
+// How: one CTA per tile of 256 tokens (128 when E > 2048; one token per
+// thread), tiles handed out in launch order by a ticket counter, so a tile's
+// predecessors are already running.  Per tile:
 //   1. each thread holds its token's K picks and weights in registers,
 //      checks them (range, no expert named twice), and sets its bit in the
-//      tile's bitmask of each picked expert (shared memory, E x 4 words);
+//      tile's bitmask of each picked expert (shared memory, E x TILE/32 words);
 //   2. per expert column: the tile's count is the popcount of its mask;
 //      decoupled look-back (Merrill & Garland, "Single-pass Parallel Prefix
 //      Scan with Decoupled Look-back", 2016) over the preceding tiles gives
@@ -33,8 +33,9 @@
 namespace ep {
 namespace {
 
-constexpr int kXTile = 128;
-constexpr int kXWords = kXTile / 32;      // mask words per expert (one per warp)
+constexpr int kXTileSmall = 128;          // tokens per tile when E is large
+constexpr int kXTileLarge = 256;          // tokens per tile when E <= kXLargeMaxE
+constexpr int kXLargeMaxE = 2048;
 constexpr int kPickBatch = 8;             // picks whose loads are in flight together
 
 struct ExpertParams {
@@ -60,8 +61,9 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&v)[8]) {
                  : "memory");
 }
 
-template <int KMAX>
-__global__ void __launch_bounds__(kXTile) expert_layout_kernel(const ExpertParams p) {
+template <int KMAX, int TILE>
+__global__ void __launch_bounds__(TILE) expert_layout_kernel(const ExpertParams p) {
+    constexpr int kXWords = TILE / 32;   // mask words per expert (one per warp)
     extern __shared__ __align__(16) uint32_t s_mask[];    // [E][kXWords], then s_excl[E]
     __shared__ unsigned long long s_ticket;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -69,12 +71,12 @@ __global__ void __launch_bounds__(kXTile) expert_layout_kernel(const ExpertParam
     int *s_excl = reinterpret_cast<int *>(s_mask + static_cast<size_t>(E) * kXWords);
 
     if (tid == 0) s_ticket = atomicAdd(p.dev.xticket, 1ull);
-    for (int i = tid; i < E * kXWords; i += kXTile) s_mask[i] = 0u;
+    for (int i = tid; i < E * kXWords; i += TILE) s_mask[i] = 0u;
     __syncthreads();
     const unsigned long long ticket = s_ticket;
     const int tile = static_cast<int>(ticket % static_cast<unsigned long long>(p.tiles));
     const uint32_t epoch = static_cast<uint32_t>((ticket / p.tiles) % ((1u << 30) - 1u)) + 1u;
-    const int64_t t = static_cast<int64_t>(tile) * kXTile + tid;
+    const int64_t t = static_cast<int64_t>(tile) * TILE + tid;
     const bool valid = t < p.T;
 
     // 1. picks and weights in registers; -1 marks "no pick" and bad picks
@@ -108,7 +110,7 @@ __global__ void __launch_bounds__(kXTile) expert_layout_kernel(const ExpertParam
 
     // 2. per expert column: publish every aggregate, then look back
     unsigned long long *desc = p.dev.xdesc + static_cast<int64_t>(tile) * E;
-    for (int e = tid; e < E; e += kXTile) {
+    for (int e = tid; e < E; e += TILE) {
         const uint32_t *m = s_mask + e * kXWords;
         int agg = 0;
 #pragma unroll
@@ -118,7 +120,7 @@ __global__ void __launch_bounds__(kXTile) expert_layout_kernel(const ExpertParam
                                          static_cast<uint32_t>(agg)));
     }
     const uint64_t t_start = globaltimer_ns();
-    for (int e = tid; e < E; e += kXTile) {
+    for (int e = tid; e < E; e += TILE) {
         const int agg = s_excl[e];
         int excl = 0;
         if (tile > 0) {
@@ -237,22 +239,28 @@ __global__ void __launch_bounds__(kXTile) expert_layout_kernel(const ExpertParam
     }
 }
 
-template <int KMAX>
+template <int KMAX, int TILE>
 cudaError_t set_smem_limit(size_t bytes) {
-    return cudaFuncSetAttribute(expert_layout_kernel<KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(expert_layout_kernel<KMAX, TILE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(bytes));
 }
 
-size_t expert_smem_bytes(int E) { return static_cast<size_t>(E) * (kXWords + 1) * 4; }
+int expert_tile(int E) { return E <= kXLargeMaxE ? kXTileLarge : kXTileSmall; }
+size_t expert_smem_bytes(int E) { return static_cast<size_t>(E) * (expert_tile(E) / 32 + 1) * 4; }
 
 }  // namespace
 
 ep_status plan_expert_layout(ep_ctx *h) {
     const int64_t T = static_cast<int64_t>(h->cfg.num_ranks) * h->cfg.tokens_per_rank;
-    h->xtiles = static_cast<int>((T + kXTile - 1) / kXTile);
-    const size_t smem = expert_smem_bytes(h->cfg.num_experts);
+    const int E = h->cfg.num_experts, tile = expert_tile(E);
+    h->xtiles = static_cast<int>((T + tile - 1) / tile);
+    const size_t smem = expert_smem_bytes(E);
     if (smem > 48 * 1024) {
-        const cudaError_t e = h->cfg.topk <= 8 ? set_smem_limit<8>(smem) : set_smem_limit<32>(smem);
+        const bool k8 = h->cfg.topk <= 8;
+        const cudaError_t e = tile == kXTileLarge ? (k8 ? set_smem_limit<8, kXTileLarge>(smem)
+                                                        : set_smem_limit<32, kXTileLarge>(smem))
+                                                  : (k8 ? set_smem_limit<8, kXTileSmall>(smem)
+                                                        : set_smem_limit<32, kXTileSmall>(smem));
         if (e != cudaSuccess) return EP_ERR_CUDA;
     }
     return EP_OK;
@@ -283,10 +291,17 @@ ep_status launch_expert_layout(ep_ctx *h, const int32_t *topk_idx, const float *
     p.vec4 = (p.K % 4 == 0 && a % 16 == 0) ? 1 : 0;
     p.vec8 = (p.K % 8 == 0 && a % 32 == 0) ? 1 : 0;
     const size_t smem = expert_smem_bytes(p.E);
-    if (p.K <= 8)
-        expert_layout_kernel<8><<<h->xtiles, kXTile, smem, st>>>(p);
-    else
-        expert_layout_kernel<32><<<h->xtiles, kXTile, smem, st>>>(p);
+    if (expert_tile(p.E) == kXTileLarge) {
+        if (p.K <= 8)
+            expert_layout_kernel<8, kXTileLarge><<<h->xtiles, kXTileLarge, smem, st>>>(p);
+        else
+            expert_layout_kernel<32, kXTileLarge><<<h->xtiles, kXTileLarge, smem, st>>>(p);
+    } else {
+        if (p.K <= 8)
+            expert_layout_kernel<8, kXTileSmall><<<h->xtiles, kXTileSmall, smem, st>>>(p);
+        else
+            expert_layout_kernel<32, kXTileSmall><<<h->xtiles, kXTileSmall, smem, st>>>(p);
+    }
     return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }
 

@@ -287,10 +287,11 @@ ep_status ep_combine_tokens(ep_handle h, const void *expert_out, int64_t expert_
  * token goes to the experts of its top-k picks, and the receiving rank runs
  * those experts on the rows it received).  Needs only the layout, not the
  * dispatched rows, so it may run on another stream while ep_dispatch moves
- * the data.  One single-pass kernel over tiles of 128 tokens: per tile a
- * bitmask of tokens per expert in shared memory, a decoupled-lookback scan
- * down each expert column giving each pick's position in its expert's
- * segment, and the per-row metadata written from the token's own picks.
+ * the data.  One single-pass kernel over tiles of 256 tokens (128 when
+ * E > 2048): per tile a bitmask of tokens per expert in shared memory, a
+ * decoupled-lookback scan down each expert column giving each pick's position
+ * in its expert's segment, and the per-row metadata written from the token's
+ * own picks.
  *  topk_idx, topk_weights: device int32 / fp32 [T, K], the inputs of
  *            ep_layout and ep_combine.  A pick outside [-1, E), or a token
  *            naming one expert twice, sets EP_ERR_INVALID_ARG on the device
@@ -302,8 +303,8 @@ ep_status ep_combine_tokens(ep_handle h, const void *expert_out, int64_t expert_
  *            (at least N); expert_rows_capacity: entries of expert_rows (at
  *            least M; T*K always suffices).  A row or an entry beyond them
  *            sets EP_ERR_CAPACITY on the device and is not written.
- * The handle's scratch for this call grows as T*E/16 bytes (the lookback
- * descriptors). */
+ * The handle's scratch for this call (the lookback descriptors) grows as
+ * T*E/32 bytes, T*E/16 when E > 2048. */
 ep_status ep_expert_layout(ep_handle h, const int32_t *topk_idx, const float *topk_weights,
                            const ep_layout_out *layout, const ep_expert_layout_out *out,
                            int64_t recv_rows, int64_t expert_rows_capacity, void *stream);
