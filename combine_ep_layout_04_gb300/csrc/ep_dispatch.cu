@@ -85,7 +85,7 @@ constexpr int kStoreLagItems = 2;   // items whose stores may still be in flight
 constexpr int kMaxPollRounds = 16;  // up to 512 slots examined per consumer step
 constexpr int kLogStage = 1024;     // staged records (16 bytes each) awaiting the logger
 constexpr uint64_t kErrCheckNs = 20000;   // idle loops read the device error word this often
-constexpr int kPosterWarpsMax = 8;        // shared-memory room for this many poster warps
+constexpr int kPosterWarpsMax = 8;        // poster warps of a channel CTA, at most
 constexpr int kListPerLane = 8;           // commands a poster lane lists per posting pass
 constexpr int kMetaLoads = 8;             // int4 token_slot loads a meta lane keeps in flight
 constexpr int kNoticeLoads = 8;           // notice entries a poster lane keeps in flight
@@ -120,16 +120,18 @@ struct SmemLayout {
     __host__ __device__ static int ranges_off(int R, int D) { return ring_off(R) + 16 * D + 16 * kLogStage; }
     __host__ __device__ static int ranges_bytes_per_warp(int R, int C) { return 32 * ((R + C - 1) / C) * 8; }
     // poster lists: per poster warp, 32 x kListPerLane packed commands
-    __host__ __device__ static int lists_off(int R, int C, int D) {
-        return (ranges_off(R, D) + kPosterWarpsMax * ranges_bytes_per_warp(R, C) + 15) & ~15;
+    __host__ __device__ static int lists_off(int R, int C, int D, int npw) {
+        return (ranges_off(R, D) + npw * ranges_bytes_per_warp(R, C) + 15) & ~15;
     }
     static constexpr int kListBytesPerWarp = 32 * kListPerLane * 16;
-    __host__ __device__ SmemLayout(int R, int C, int D, int stage_bytes, int stages) {
+    // npw: the poster warps that run (fewer when their ranges would not fit
+    // beside the ring, e.g. 64 destinations on one channel)
+    __host__ __device__ SmemLayout(int R, int C, int D, int stage_bytes, int stages, int npw) {
         stage_off = 0;
         // channel CTAs keep the pair tables (3 x R x R ints) and their ring
         // (D slots of 16 bytes) where copy CTAs keep their stages
         const int stage_area = stage_bytes * stages,
-                  channel = lists_off(R, C, D) + kPosterWarpsMax * kListBytesPerWarp;
+                  channel = lists_off(R, C, D, npw) + npw * kListBytesPerWarp;
         meta_off = stage_area > channel ? stage_area : channel;
         meta_slot_bytes = ((32 * R + 33) + 3) / 4 * 16;   // dst[32*R] | pref[33]
         scratch_off = meta_off + meta_slot_bytes * kMetaSlots;
@@ -721,7 +723,7 @@ __device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long
     bool failed = false;
     const int ngroups = nd > 0 ? (p.k1 - p.k0 + 31) / 32 : 0;
     uint64_t err_checked = globaltimer_ns();
-    for (int grp = w; grp < ngroups && !failed; grp += kPosterWarps) {
+    for (int grp = w; grp < ngroups && !failed; grp += p.poster_warps) {
         const int k = p.k0 + grp * 32 + lane;
         // Post the group's chunks as they become ready: wait until at least
         // one pending chunk's flag is set (polling device memory with a
@@ -1056,7 +1058,7 @@ __device__ void consumer_log(const DispatchParams &p, int c, long long expected,
 
 __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    const SmemLayout L(p.R, p.C, p.D, p.stage_bytes, p.stages);
+    const SmemLayout L(p.R, p.C, p.D, p.stage_bytes, p.stages, p.poster_warps);
     int *rbase = reinterpret_cast<int *>(smem + L.scratch_off);
     unsigned long long *words =
         reinterpret_cast<unsigned long long *>(smem + L.scratch_off + ((p.R + 3) & ~3) * 4);
@@ -1150,7 +1152,9 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
                 pt.send0 = pt.recv0 + p.R * p.R;
                 const int pw = poster_index(warp);
                 uint8_t *rb = smem + SmemLayout::ranges_off(p.R, p.D) + pw * SmemLayout::ranges_bytes_per_warp(p.R, p.C);
-                uint8_t *lb = smem + SmemLayout::lists_off(p.R, p.C, p.D) + pw * SmemLayout::kListBytesPerWarp;
+                uint8_t *lb =
+                    smem + SmemLayout::lists_off(p.R, p.C, p.D, p.poster_warps) + pw * SmemLayout::kListBytesPerWarp;
+                if (pw < p.poster_warps)
                 poster_warp(p, c, pw, words, pt, reinterpret_cast<unsigned long long *>(smem + SmemLayout::ring_off(p.R)),
                             reinterpret_cast<int2 *>(rb), reinterpret_cast<unsigned long long *>(lb));
             } else if (!(p.debug & EP_DEBUG_DISABLE_CONSUMER)) {
@@ -1220,16 +1224,21 @@ ep_status plan_dispatch(ep_ctx *h) {
     if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device) != cudaSuccess)
         return EP_ERR_CUDA;
     const int reserve = 1024;   // static + alignment slack
-    int stages = 0;
-    for (int s = kStagesMax; s >= 3; --s) {
-        SmemLayout L(R, C, h->cfg.ring_depth, stage_bytes, s);
-        if (L.total + reserve <= max_smem) {
-            stages = s;
-            break;
+    // the most poster warps that fit, then the most stages
+    int stages = 0, npw = kPosterWarpsMax;
+    for (; npw >= 1 && stages == 0; npw /= 2) {
+        for (int s = kStagesMax; s >= 3; --s) {
+            SmemLayout L(R, C, h->cfg.ring_depth, stage_bytes, s, npw);
+            if (L.total + reserve <= max_smem) {
+                stages = s;
+                break;
+            }
         }
+        if (stages) break;
     }
     if (stages == 0) return EP_ERR_INVALID_ARG;
-    SmemLayout L(R, C, h->cfg.ring_depth, stage_bytes, stages);
+    SmemLayout L(R, C, h->cfg.ring_depth, stage_bytes, stages, npw);
+    h->poster_warps = npw;
     h->rows_per_item = rows_per_item;
     h->vec_store = (pieces == 1 && B <= kVecRowMax) ? 1 : 0;
     h->pieces = pieces;
@@ -1300,6 +1309,7 @@ ep_status launch_dispatch(ep_ctx *h, const void *x, const ep_layout_out *lay, vo
     p.slot_vec = (p.R % 4 == 0 && reinterpret_cast<uintptr_t>(lay->token_slot) % 16 == 0) ? 1 : 0;
     p.lg_depth = __builtin_ctz(static_cast<unsigned>(p.D));
     p.vec_store = h->vec_store;
+    p.poster_warps = h->poster_warps;
     p.store_warps = kThreads / 32 - kStoreWarp0;
     void *args[] = {&p};
     const cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(dispatch_kernel),

@@ -93,6 +93,7 @@ struct DispatchParams {
     int slot_vec;        // 1: token_slot rows are 16-byte aligned (int4 loads)
     int vec_store;       // 1: rows leave shared memory by the store warps' vector stores
     int store_warps;     // store warps per copy CTA on that path
+    int poster_warps;    // poster warps per channel CTA that run (1..8)
     int lg_depth;        // log2(D)
 };
 
@@ -131,6 +132,7 @@ struct ep_ctx {
     int rows_per_item, pieces, piece_bytes;
     int chunks_per_rank, nchunks, chunk_tokens;
     int vec_store;
+    int poster_warps;
     int64_t log_cap;
     // combine geometry
     int comb_grid, comb_threads;

@@ -141,6 +141,13 @@ def test_ring_options(opts):
     run_and_check(w, **opts)
 
 
+def test_many_destinations_per_channel():
+    # 64 ranks on one ring: the posters' per-destination ranges then take so
+    # much shared memory that fewer poster warps run
+    w = _w(num_ranks=64, tokens_per_rank=9, hidden=2056, num_experts=448, topk=8)
+    run_and_check(w, channels=1, ring_depth=256, max_inflight=8, batch=2, rows_per_msg=3)
+
+
 def test_small_rings_wrap_many_times():
     w = W.get("small")
     run_and_check(w, ring_depth=32, max_inflight=16, identity_check=False, sample_tokens=256)
