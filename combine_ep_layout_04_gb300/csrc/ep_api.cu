@@ -10,6 +10,29 @@
 
 using ep::DevState;
 
+namespace ep {
+
+// True if the kernels may dereference p on `device`: memory of that device,
+// managed memory, or page-locked host memory mapped into the device's address
+// space.  Pageable host memory, memory of another device and addresses the
+// runtime does not know are refused, so that a wrong pointer is an
+// EP_ERR_INVALID_ARG on the host instead of a fault on the GPU.
+bool ptr_usable_on(int device, const void *p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();   // not sticky; leave no error behind
+        return false;
+    }
+    switch (a.type) {
+    case cudaMemoryTypeDevice: return a.device == device && a.devicePointer != nullptr;
+    case cudaMemoryTypeManaged: return true;
+    case cudaMemoryTypeHost: return a.devicePointer != nullptr;
+    default: return false;
+    }
+}
+
+}  // namespace ep
+
 namespace {
 
 bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
@@ -26,6 +49,31 @@ constexpr uint64_t kMaxWaitNs = 10000000000ull;   // longest ep_wait_signal: 10 
 bool layout_ptrs_ok(const ep_layout_out *o) {
     return o && o->num_tokens_per_expert && o->num_tokens_per_rank && o->is_token_in_rank && o->token_slot &&
            o->recv_off && o->send_off && o->msg_count && o->recv_count && o->recv_base && o->expert_off;
+}
+
+// The same check through a small per-thread cache keyed by device and
+// pointer value: callers pass the same buffers call after call, so the
+// runtime is asked once per buffer.
+bool ptr_usable(ep_ctx *h, const void *p) {
+    constexpr int kSlots = 64;
+    struct Slot {
+        uintptr_t ptr;
+        int device;
+    };
+    thread_local Slot cache[kSlots] = {};
+    const uintptr_t v = reinterpret_cast<uintptr_t>(p);
+    Slot &slot = cache[((v >> 8) ^ (v >> 20)) % kSlots];
+    if (slot.ptr == v && slot.device == h->device) return true;
+    if (!ep::ptr_usable_on(h->device, p)) return false;
+    slot = Slot{v, h->device};
+    return true;
+}
+
+bool layout_ptrs_usable(ep_ctx *h, const ep_layout_out *o) {
+    return ptr_usable(h, o->num_tokens_per_expert) && ptr_usable(h, o->num_tokens_per_rank) &&
+           ptr_usable(h, o->is_token_in_rank) && ptr_usable(h, o->token_slot) && ptr_usable(h, o->recv_off) &&
+           ptr_usable(h, o->send_off) && ptr_usable(h, o->msg_count) && ptr_usable(h, o->recv_count) &&
+           ptr_usable(h, o->recv_base) && ptr_usable(h, o->expert_off);
 }
 
 // Carves one allocation into 256-byte aligned pieces.
@@ -217,6 +265,7 @@ ep_status ep_reset(ep_handle h) {
 ep_status ep_layout(ep_handle h, const int32_t *topk_idx, const ep_layout_out *out, int64_t *n_recv_host,
                     void *stream) {
     if (!h || !topk_idx || !layout_ptrs_ok(out)) return EP_ERR_INVALID_ARG;
+    if (!ptr_usable(h, topk_idx) || !layout_ptrs_usable(h, out)) return EP_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     ep_status s = ep::launch_layout(h, topk_idx, out, st);
     if (s != EP_OK || !n_recv_host) return s;
@@ -233,6 +282,7 @@ ep_status ep_dispatch_ranks(ep_handle h, const void *x, const ep_layout_out *lay
     if (!h || !x || !recv || !layout_ptrs_ok(layout) || recv_capacity_rows < 0) return EP_ERR_INVALID_ARG;
     if (src_begin < 0 || src_end < src_begin || src_end > h->cfg.num_ranks) return EP_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(recv)) return EP_ERR_INVALID_ARG;
+    if (!ptr_usable(h, x) || !ptr_usable(h, recv) || !layout_ptrs_usable(h, layout)) return EP_ERR_INVALID_ARG;
     return ep::launch_dispatch(h, x, layout, recv, recv_capacity_rows, src_begin, src_end,
                                static_cast<cudaStream_t>(stream));
 }
@@ -250,6 +300,9 @@ ep_status ep_combine_tokens(ep_handle h, const void *expert_out, int64_t expert_
     const int64_t T = static_cast<int64_t>(h->cfg.num_ranks) * h->cfg.tokens_per_rank;
     if (t_begin < 0 || t_end < t_begin || t_end > T) return EP_ERR_INVALID_ARG;
     if (!aligned16(expert_out) || !aligned16(out)) return EP_ERR_INVALID_ARG;
+    if (!ptr_usable(h, expert_out) || !ptr_usable(h, topk_weights) || !ptr_usable(h, topk_idx) ||
+        !ptr_usable(h, out) || !layout_ptrs_usable(h, layout))
+        return EP_ERR_INVALID_ARG;
     return ep::launch_combine(h, expert_out, expert_out_rows, topk_weights, topk_idx, layout, out, t_begin, t_end,
                               static_cast<cudaStream_t>(stream));
 }
@@ -266,6 +319,10 @@ ep_status ep_expert_layout(ep_handle h, const int32_t *topk_idx, const float *to
     if (!h || !topk_idx || !topk_weights || !layout_ptrs_ok(layout) || !out || !out->recv_topk_idx ||
         !out->recv_topk_weights || !out->recv_src_token || !out->expert_rows || !out->expert_count ||
         recv_rows < 0 || expert_rows_capacity < 0)
+        return EP_ERR_INVALID_ARG;
+    if (!ptr_usable(h, topk_idx) || !ptr_usable(h, topk_weights) || !layout_ptrs_usable(h, layout) ||
+        !ptr_usable(h, out->recv_topk_idx) || !ptr_usable(h, out->recv_topk_weights) ||
+        !ptr_usable(h, out->recv_src_token) || !ptr_usable(h, out->expert_rows) || !ptr_usable(h, out->expert_count))
         return EP_ERR_INVALID_ARG;
     return ep::launch_expert_layout(h, topk_idx, topk_weights, layout, out, recv_rows, expert_rows_capacity,
                                     static_cast<cudaStream_t>(stream));
@@ -294,6 +351,7 @@ ep_status ep_wait_signal(ep_handle h, int32_t dst_rank, uint64_t expected, uint6
                          void *stream) {
     if (!h || !status_out || dst_rank < 0 || dst_rank >= h->cfg.num_ranks || timeout_ns > kMaxWaitNs)
         return EP_ERR_INVALID_ARG;
+    if (!ptr_usable(h, status_out)) return EP_ERR_INVALID_ARG;
     return ep::launch_wait_signal(h->dev.signal + dst_rank, expected, timeout_ns, status_out,
                                   static_cast<cudaStream_t>(stream));
 }

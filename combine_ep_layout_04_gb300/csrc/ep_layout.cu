@@ -358,6 +358,9 @@ ep_status launch_layout(ep_ctx *h, const int32_t *topk_idx, const ep_layout_out 
 #include <mutex>
 
 namespace ep {
+
+bool ptr_usable_on(int device, const void *p);   // ep_api.cu: may the kernels dereference p?
+
 namespace {
 
 constexpr int kStaticMaxTokens = 262144;   // T = num_ranks * tokens_per_rank
@@ -407,6 +410,15 @@ extern "C" ep_status ep_layout_static(const ep_config *cfg, const int32_t *topk_
     const int64_t T = static_cast<int64_t>(cfg->num_ranks) * cfg->tokens_per_rank;
     if (T > kStaticMaxTokens || cfg->num_ranks > kStaticMaxRanks || cfg->num_experts > kStaticMaxExperts)
         return EP_ERR_CAPACITY;   // beyond what the fixed scratch holds
+    {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return EP_ERR_CUDA;
+        const void *ptrs[] = {topk_idx, out->num_tokens_per_expert, out->num_tokens_per_rank, out->is_token_in_rank,
+                              out->token_slot, out->recv_off, out->send_off, out->msg_count, out->recv_count,
+                              out->recv_base, out->expert_off};
+        for (const void *q : ptrs)
+            if (!ptr_usable_on(dev, q)) return EP_ERR_INVALID_ARG;
+    }
     void *base = nullptr;
     const ep_status st0 = static_scratch(&base);
     if (st0 != EP_OK) return st0;

@@ -5,6 +5,7 @@ kernels (layout, dispatch with its TransferCmd rings, combine)."""
 from __future__ import annotations
 
 import dataclasses
+import weakref
 
 import numpy as np
 import torch
@@ -77,6 +78,23 @@ def _stream(device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
 
 
+def check_tensor(t, name: str, dtype: torch.dtype, device: torch.device, shape=None) -> None:
+    """Raise unless t is a contiguous `dtype` tensor on `device` whose shape
+    matches `shape` (None entries match any size).  The kernels index these
+    buffers by the layer's sizes, so a wrong one must not reach them."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if t.device != device:
+        raise ValueError(f"{name}: on {t.device}, the layer is on {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if shape is not None and (t.dim() != len(shape) or
+                              any(want is not None and got != want for got, want in zip(t.shape, shape))):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple('*' if v is None else v for v in shape)}")
+
+
 class EpLayer:
     """One EP layer: R simulated ranks in this GPU's memory."""
 
@@ -119,6 +137,25 @@ class EpLayer:
         self.close()
 
     # -- the three calls
+    def _layout_shapes(self) -> dict:
+        R, T, E = self.R, self.T, self.E
+        return {"num_tokens_per_expert": (R, E), "num_tokens_per_rank": (R, R), "is_token_in_rank": (T, R),
+                "token_slot": (T, R), "recv_off": (R, R), "send_off": (R, R), "msg_count": (R, R),
+                "recv_count": (R,), "recv_base": (R,), "expert_off": (E,)}
+
+    def _check_layout(self, lay: Layout) -> None:
+        """Shapes, dtypes and device of a Layout's tensors, checked once per
+        Layout object (a Layout that passed is marked with this layer)."""
+        if not isinstance(lay, Layout):
+            raise TypeError(f"expected a Layout, got {type(lay).__name__}")
+        ref = getattr(lay, "_checked_by", None)
+        if ref is not None and ref() is self:
+            return
+        for f, shape in self._layout_shapes().items():
+            check_tensor(getattr(lay, f), f, torch.uint8 if f == "is_token_in_rank" else torch.int32,
+                         self.device, shape)
+        lay._checked_by = weakref.ref(self)   # no strong reference: the layer may go first
+
     def alloc_layout(self) -> Layout:
         R, T, E = self.R, self.T, self.E
         i32 = dict(dtype=torch.int32, device=self.device)
@@ -130,8 +167,9 @@ class EpLayer:
     def layout(self, topk_idx: torch.Tensor, out: Layout | None = None, sync: bool = True) -> Layout:
         """ep_layout.  topk_idx: int32 [T, K] on the device.  With sync=True the
         call waits for N (n_recv) so that the caller can size recv."""
-        assert topk_idx.dtype == torch.int32 and topk_idx.is_contiguous() and topk_idx.shape == (self.T, self.K)
+        check_tensor(topk_idx, "topk_idx", torch.int32, self.device, (self.T, self.K))
         out = self.alloc_layout() if out is None else out
+        self._check_layout(out)
         out.n_recv = _ep.ep_layout(self.handle, topk_idx.data_ptr(), out.struct(), _stream(self.device), want_n=sync)
         return out
 
@@ -139,12 +177,13 @@ class EpLayer:
                  src_ranks: tuple[int, int] | None = None) -> torch.Tensor:
         """ep_dispatch (ep_dispatch_ranks for src_ranks=(begin, end)).
         x: bf16 [T, H].  Returns recv bf16 [capacity, H]."""
-        assert x.dtype == torch.bfloat16 and x.is_contiguous() and x.shape == (self.T, self.H)
+        check_tensor(x, "x", torch.bfloat16, self.device, (self.T, self.H))
+        self._check_layout(lay)
         if recv is None:
             if lay.n_recv is None:
                 raise ValueError("dispatch needs recv or a layout computed with sync=True")
             recv = torch.empty((lay.n_recv, self.H), dtype=torch.bfloat16, device=self.device)
-        assert recv.dtype == torch.bfloat16 and recv.is_contiguous() and recv.shape[1] == self.H
+        check_tensor(recv, "recv", torch.bfloat16, self.device, (None, self.H))
         if src_ranks is None:
             _ep.ep_dispatch(self.handle, x.data_ptr(), lay.struct(), recv.data_ptr(), recv.shape[0],
                             _stream(self.device))
@@ -157,11 +196,13 @@ class EpLayer:
                 out: torch.Tensor | None = None, tokens: tuple[int, int] | None = None) -> torch.Tensor:
         """ep_combine (ep_combine_tokens for tokens=(begin, end)).
         expert_out: bf16 [rows, H]; topk_weights fp32 [T, K]."""
-        assert expert_out.dtype == torch.bfloat16 and expert_out.is_contiguous() and expert_out.shape[1] == self.H
-        assert topk_weights.dtype == torch.float32 and topk_weights.is_contiguous()
-        assert topk_idx.dtype == torch.int32 and topk_idx.is_contiguous()
+        check_tensor(expert_out, "expert_out", torch.bfloat16, self.device, (None, self.H))
+        check_tensor(topk_weights, "topk_weights", torch.float32, self.device, (self.T, self.K))
+        check_tensor(topk_idx, "topk_idx", torch.int32, self.device, (self.T, self.K))
+        self._check_layout(lay)
         if out is None:
             out = torch.empty((self.T, self.H), dtype=torch.bfloat16, device=self.device)
+        check_tensor(out, "out", torch.bfloat16, self.device, (self.T, self.H))
         if tokens is None:
             _ep.ep_combine(self.handle, expert_out.data_ptr(), expert_out.shape[0], topk_weights.data_ptr(),
                            topk_idx.data_ptr(), lay.struct(), out.data_ptr(), _stream(self.device))
@@ -176,9 +217,9 @@ class EpLayer:
         """ep_expert_layout: per receive row its source token and local picks
         and weights; per expert its receive rows.  Needs N (a layout computed
         with sync=True) unless `out` is given."""
-        assert topk_idx.dtype == torch.int32 and topk_idx.is_contiguous() and topk_idx.shape == (self.T, self.K)
-        assert topk_weights.dtype == torch.float32 and topk_weights.is_contiguous()
-        assert topk_weights.shape == (self.T, self.K)
+        check_tensor(topk_idx, "topk_idx", torch.int32, self.device, (self.T, self.K))
+        check_tensor(topk_weights, "topk_weights", torch.float32, self.device, (self.T, self.K))
+        self._check_layout(lay)
         if out is None:
             if lay.n_recv is None:
                 raise ValueError("expert_layout needs `out` or a layout computed with sync=True")
@@ -187,6 +228,14 @@ class EpLayer:
             out = ExpertLayout(torch.empty((N, K), **i32), torch.empty((N, K), dtype=torch.float32, device=self.device),
                                torch.empty((N,), **i32), torch.empty((self.T * K,), **i32),
                                torch.empty((self.E,), **i32))
+        if not isinstance(out, ExpertLayout):
+            raise TypeError(f"out: expected an ExpertLayout, got {type(out).__name__}")
+        n = out.recv_src_token.shape[0] if isinstance(out.recv_src_token, torch.Tensor) else None
+        check_tensor(out.recv_src_token, "recv_src_token", torch.int32, self.device, (None,))
+        check_tensor(out.recv_topk_idx, "recv_topk_idx", torch.int32, self.device, (n, self.K))
+        check_tensor(out.recv_topk_weights, "recv_topk_weights", torch.float32, self.device, (n, self.K))
+        check_tensor(out.expert_rows, "expert_rows", torch.int32, self.device, (None,))
+        check_tensor(out.expert_count, "expert_count", torch.int32, self.device, (self.E,))
         _ep.ep_expert_layout(self.handle, topk_idx.data_ptr(), topk_weights.data_ptr(), lay.struct(), out.struct(),
                              out.recv_src_token.shape[0], out.expert_rows.shape[0], _stream(self.device))
         return out
@@ -206,7 +255,9 @@ class EpLayer:
     def wait_signal(self, dst_rank: int, expected: int, timeout_ns: int, status: torch.Tensor) -> torch.Tensor:
         """ep_wait_signal: enqueue a bounded wait; `status` (device int32 [1])
         receives EP_OK or EP_ERR_NOT_READY."""
-        assert status.dtype == torch.int32 and status.device == self.device
+        check_tensor(status, "status", torch.int32, self.device, (None,))
+        if status.numel() < 1:
+            raise ValueError("status: needs at least one element")
         _ep.ep_wait_signal(self.handle, dst_rank, expected, timeout_ns, status.data_ptr(), _stream(self.device))
         return status
 

@@ -12,7 +12,14 @@
  *
  * Conventions for every call:
  *  - All tensor arguments are DEVICE pointers owned by the caller (e.g. torch
- *    allocations); the library never frees them.  Row-major, dense.
+ *    allocations); the library never frees them.  Row-major, dense.  Each
+ *    call asks the CUDA runtime what every pointer is (cached per host thread
+ *    by device and pointer value) and accepts memory of the handle's device,
+ *    managed memory and page-locked host memory mapped into the device's
+ *    address space; pageable host memory, another device's memory and unknown
+ *    addresses are EP_ERR_INVALID_ARG before anything is launched.  Buffer
+ *    sizes cannot be checked this way: they must be at least what each call
+ *    states.
  *  - bf16 tensors are passed as void* holding IEEE bfloat16 bits.
  *  - Device pointers of row data (x, recv, expert_out, out) must be 16-byte
  *    aligned; hidden must be a multiple of 8 (rows are whole 16-byte units).

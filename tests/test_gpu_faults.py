@@ -116,6 +116,49 @@ def test_host_argument_checks():
         assert layer.device_status() == 0
 
 
+def test_pointer_kinds_checked_on_the_host():
+    """The C ABI refuses pageable host memory before any launch and accepts
+    page-locked host memory, which the kernels read through its device
+    mapping; the binding refuses tensors on the wrong device or of the wrong
+    shape before calling the library."""
+    from combine_ep_layout_04_gb300 import _ep
+    w = _w()
+    stream = torch.cuda.current_stream().cuda_stream
+    with _layer(w) as layer:
+        idx, wt = W.make_routing(w)
+        ref = layer.layout(torch.from_numpy(idx).cuda()).numpy()
+        lay = layer.alloc_layout()
+        pageable = np.ascontiguousarray(idx)
+        assert _ep.lib.ep_layout(layer.handle, pageable.ctypes.data, lay.struct(), None, stream) == \
+            _ep.EP_ERR_INVALID_ARG
+        torch.cuda.synchronize()
+        assert layer.device_status() == 0
+        pinned = torch.from_numpy(idx).pin_memory()
+        n = _ep.ep_layout(layer.handle, pinned.data_ptr(), lay.struct(), stream, want_n=True)
+        assert n == ref["n_recv"]
+        got = lay.numpy()
+        for k in ref:
+            if k != "n_recv":
+                assert np.array_equal(got[k], ref[k]), k
+        with pytest.raises(ValueError):
+            layer.layout(torch.from_numpy(idx))                      # host tensor
+        with pytest.raises(TypeError):
+            layer.layout(torch.from_numpy(idx).cuda().long())         # int64 picks
+        x = torch.randn(w.num_tokens, w.hidden, device="cuda").to(torch.bfloat16)
+        lay2 = layer.layout(torch.from_numpy(idx).cuda())
+        recv = layer.dispatch(x, lay2)
+        wts = torch.from_numpy(wt).cuda()
+        topk = torch.from_numpy(idx).cuda()
+        with pytest.raises(ValueError):
+            layer.combine(recv, wts, topk, lay2, out=torch.empty((w.num_tokens - 1, w.hidden), dtype=torch.bfloat16,
+                                                                    device="cuda"))
+        bad = layer.alloc_layout()
+        bad.token_slot = bad.token_slot[:-1]
+        with pytest.raises(ValueError):
+            layer.layout(topk, out=bad)
+        assert layer.device_status() == 0
+
+
 def test_cuda_graph_replay():
     w = W.get("small")
     idx, wt = W.make_routing(w)
