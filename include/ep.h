@@ -17,9 +17,11 @@
  *    by device and pointer value) and accepts memory of the handle's device,
  *    managed memory and page-locked host memory mapped into the device's
  *    address space; pageable host memory, another device's memory and unknown
- *    addresses are EP_ERR_INVALID_ARG before anything is launched.  Buffer
- *    sizes cannot be checked this way: they must be at least what each call
- *    states.
+ *    addresses are EP_ERR_INVALID_ARG before anything is launched (an
+ *    address found usable once is not asked about again on that thread, so
+ *    a buffer freed and its address reused for another kind of memory slips
+ *    through).  Buffer sizes cannot be checked this way: they must be at
+ *    least what each call states.
  *  - bf16 tensors are passed as void* holding IEEE bfloat16 bits.
  *  - Device pointers of row data (x, recv, expert_out, out) must be 16-byte
  *    aligned; hidden must be a multiple of 8 (rows are whole 16-byte units).
