@@ -44,6 +44,29 @@ int default_rows_per_msg(int hidden) { return 2 * hidden < 7 * 1024 ? 8 : 1; }
 
 ep_status cuda_ok(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
 
+// Makes the handle's device current for one call and then puts the caller's
+// back, so that a call made while another device is current still launches
+// where the handle's memory lives.
+struct DeviceGuard {
+    int prev = -1;
+    bool switched = false, ok = true;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) {
+            ok = false;
+            return;
+        }
+        if (prev != dev) {
+            ok = cudaSetDevice(dev) == cudaSuccess;
+            switched = ok;
+        }
+    }
+    ~DeviceGuard() {
+        if (switched) (void)cudaSetDevice(prev);
+    }
+    DeviceGuard(const DeviceGuard &) = delete;
+    DeviceGuard &operator=(const DeviceGuard &) = delete;
+};
+
 constexpr uint64_t kMaxWaitNs = 10000000000ull;   // longest ep_wait_signal: 10 s
 
 bool layout_ptrs_ok(const ep_layout_out *o) {
@@ -243,6 +266,8 @@ ep_status ep_create(const ep_config *cfg, ep_handle *out) {
 
 ep_status ep_destroy(ep_handle h) {
     if (!h) return EP_ERR_INVALID_ARG;
+    DeviceGuard dg(h->device);
+    if (!dg.ok) return EP_ERR_CUDA;
     const cudaError_t e1 = cudaDeviceSynchronize();
     const cudaError_t e2 = cudaFree(h->alloc_base);
     delete h;
@@ -251,12 +276,16 @@ ep_status ep_destroy(ep_handle h) {
 
 ep_status ep_last_device_status(ep_handle h, int32_t *code) {
     if (!h || !code) return EP_ERR_INVALID_ARG;
+    DeviceGuard dg(h->device);
+    if (!dg.ok) return EP_ERR_CUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return EP_ERR_CUDA;
     return cuda_ok(cudaMemcpy(code, h->dev.err, sizeof(int32_t), cudaMemcpyDeviceToHost));
 }
 
 ep_status ep_reset(ep_handle h) {
     if (!h) return EP_ERR_INVALID_ARG;
+    DeviceGuard dg(h->device);
+    if (!dg.ok) return EP_ERR_CUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return EP_ERR_CUDA;
     if (cudaMemset(h->alloc_base, 0, h->alloc_bytes) != cudaSuccess) return EP_ERR_CUDA;
     return cuda_ok(cudaDeviceSynchronize());
@@ -265,6 +294,8 @@ ep_status ep_reset(ep_handle h) {
 ep_status ep_layout(ep_handle h, const int32_t *topk_idx, const ep_layout_out *out, int64_t *n_recv_host,
                     void *stream) {
     if (!h || !topk_idx || !layout_ptrs_ok(out)) return EP_ERR_INVALID_ARG;
+    DeviceGuard dg(h->device);
+    if (!dg.ok) return EP_ERR_CUDA;
     if (!ptr_usable(h, topk_idx) || !layout_ptrs_usable(h, out)) return EP_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     ep_status s = ep::launch_layout(h, topk_idx, out, st);
@@ -280,6 +311,8 @@ ep_status ep_layout(ep_handle h, const int32_t *topk_idx, const ep_layout_out *o
 ep_status ep_dispatch_ranks(ep_handle h, const void *x, const ep_layout_out *layout, void *recv,
                             int64_t recv_capacity_rows, int32_t src_begin, int32_t src_end, void *stream) {
     if (!h || !x || !recv || !layout_ptrs_ok(layout) || recv_capacity_rows < 0) return EP_ERR_INVALID_ARG;
+    DeviceGuard dg(h->device);
+    if (!dg.ok) return EP_ERR_CUDA;
     if (src_begin < 0 || src_end < src_begin || src_end > h->cfg.num_ranks) return EP_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(recv)) return EP_ERR_INVALID_ARG;
     if (!ptr_usable(h, x) || !ptr_usable(h, recv) || !layout_ptrs_usable(h, layout)) return EP_ERR_INVALID_ARG;
@@ -297,6 +330,8 @@ ep_status ep_combine_tokens(ep_handle h, const void *expert_out, int64_t expert_
                             int64_t t_end, void *stream) {
     if (!h || !expert_out || !topk_weights || !topk_idx || !layout_ptrs_ok(layout) || !out || expert_out_rows < 0)
         return EP_ERR_INVALID_ARG;
+    DeviceGuard dg(h->device);
+    if (!dg.ok) return EP_ERR_CUDA;
     const int64_t T = static_cast<int64_t>(h->cfg.num_ranks) * h->cfg.tokens_per_rank;
     if (t_begin < 0 || t_end < t_begin || t_end > T) return EP_ERR_INVALID_ARG;
     if (!aligned16(expert_out) || !aligned16(out)) return EP_ERR_INVALID_ARG;
@@ -320,6 +355,8 @@ ep_status ep_expert_layout(ep_handle h, const int32_t *topk_idx, const float *to
         !out->recv_topk_weights || !out->recv_src_token || !out->expert_rows || !out->expert_count ||
         recv_rows < 0 || expert_rows_capacity < 0)
         return EP_ERR_INVALID_ARG;
+    DeviceGuard dg(h->device);
+    if (!dg.ok) return EP_ERR_CUDA;
     if (!ptr_usable(h, topk_idx) || !ptr_usable(h, topk_weights) || !layout_ptrs_usable(h, layout) ||
         !ptr_usable(h, out->recv_topk_idx) || !ptr_usable(h, out->recv_topk_weights) ||
         !ptr_usable(h, out->recv_src_token) || !ptr_usable(h, out->expert_rows) || !ptr_usable(h, out->expert_count))
@@ -336,6 +373,8 @@ ep_status ep_signal_ptr(ep_handle h, const uint64_t **signals) {
 
 ep_status ep_signal_get(ep_handle h, uint64_t *host_out, int32_t n) {
     if (!h || !host_out || n < 0 || n > h->cfg.num_ranks) return EP_ERR_INVALID_ARG;
+    DeviceGuard dg(h->device);
+    if (!dg.ok) return EP_ERR_CUDA;
     if (n == 0) return EP_OK;
     if (cudaDeviceSynchronize() != cudaSuccess) return EP_ERR_CUDA;
     return cuda_ok(cudaMemcpy(host_out, h->dev.signal, sizeof(uint64_t) * n, cudaMemcpyDeviceToHost));
@@ -343,6 +382,8 @@ ep_status ep_signal_get(ep_handle h, uint64_t *host_out, int32_t n) {
 
 ep_status ep_signal_reset(ep_handle h, void *stream) {
     if (!h) return EP_ERR_INVALID_ARG;
+    DeviceGuard dg(h->device);
+    if (!dg.ok) return EP_ERR_CUDA;
     return cuda_ok(cudaMemsetAsync(h->dev.signal, 0, sizeof(uint64_t) * h->cfg.num_ranks,
                                    static_cast<cudaStream_t>(stream)));
 }
@@ -351,6 +392,8 @@ ep_status ep_wait_signal(ep_handle h, int32_t dst_rank, uint64_t expected, uint6
                          void *stream) {
     if (!h || !status_out || dst_rank < 0 || dst_rank >= h->cfg.num_ranks || timeout_ns > kMaxWaitNs)
         return EP_ERR_INVALID_ARG;
+    DeviceGuard dg(h->device);
+    if (!dg.ok) return EP_ERR_CUDA;
     if (!ptr_usable(h, status_out)) return EP_ERR_INVALID_ARG;
     return ep::launch_wait_signal(h->dev.signal + dst_rank, expected, timeout_ns, status_out,
                                   static_cast<cudaStream_t>(stream));
@@ -367,6 +410,8 @@ ep_status ep_cmd_log_get(ep_handle h, ep_cmd_log *out) {
 
 ep_status ep_ring_stats_get(ep_handle h, ep_ring_stats *out, int32_t n) {
     if (!h || !out || n < 0 || n > h->cfg.channels) return EP_ERR_INVALID_ARG;
+    DeviceGuard dg(h->device);
+    if (!dg.ok) return EP_ERR_CUDA;
     if (n == 0) return EP_OK;
     if (cudaDeviceSynchronize() != cudaSuccess) return EP_ERR_CUDA;
     const int C = h->cfg.channels;
@@ -404,6 +449,8 @@ ep_status ep_ring_stats_get(ep_handle h, ep_ring_stats *out, int32_t n) {
 
 ep_status ep_check_completion(ep_handle h, int32_t channel, uint64_t cmd_idx) {
     if (!h || channel < 0 || channel >= h->cfg.channels) return EP_ERR_INVALID_ARG;
+    DeviceGuard dg(h->device);
+    if (!dg.ok) return EP_ERR_CUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return EP_ERR_CUDA;
     unsigned long long tail = 0;
     if (cudaMemcpy(&tail, h->dev.tail + static_cast<size_t>(channel) * ep::kHeadStride, sizeof(tail),

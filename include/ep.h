@@ -25,7 +25,9 @@
  *  - bf16 tensors are passed as void* holding IEEE bfloat16 bits.
  *  - Device pointers of row data (x, recv, expert_out, out) must be 16-byte
  *    aligned; hidden must be a multiple of 8 (rows are whole 16-byte units).
- *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream)
+ *    of the handle's device.  A call on a handle makes that device current
+ *    while it runs and then restores the caller's current device.
  *    Work is enqueued on it and the call returns without waiting, except where
  *    a call says it synchronises.
  *  - Every call returns an ep_status.  Arguments are checked on the host before
