@@ -138,3 +138,21 @@ def test_combine_rejects_rows_outside_expert_out():
     eo = np.zeros((lay["n_recv"] - 1, w.hidden), np.uint16)
     with pytest.raises(oracle.OracleError):
         oracle.combine(lay, idx, wt, w.experts_per_rank, eo)
+
+
+def test_worked_example(golden):
+    """A combine worked out by hand (tests/golden/combine_worked_example.txt):
+    ties to even both ways, a negative tie, an exact cancellation to +0, a
+    round up, and two picks on one rank reading the same row."""
+    g = golden("combine_worked_example.txt")
+    R, Tpr, E, K, H = g["R"][0], g["tokens_per_rank"][0], g["E"][0], g["K"][0], g["H"][0]
+    idx = np.array(g["topk_idx"], np.int32).reshape(R * Tpr, K)
+    wts = np.array(g["topk_weight_bits"], np.uint32).view(np.float32).reshape(R * Tpr, K)
+    lay = oracle.layout(R, Tpr, E, idx, oracle.default_rows_per_msg(H))
+    assert lay["token_slot"].ravel().tolist() == g["token_slot"]
+    assert lay["recv_base"].tolist() == g["recv_base"]
+    eo = np.array(g["expert_out_bits"], np.uint16)
+    want = np.array(g["out_bits"], np.uint16)
+    assert np.array_equal(oracle.combine(lay, idx, wts, E // R, eo), want)
+    assert np.array_equal(brute.combine(lay, idx, wts, E // R, eo), want)
+
