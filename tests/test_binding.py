@@ -4,12 +4,18 @@ the library is called."""
 import pytest
 import torch
 
-from combine_ep_layout_04_gb300.layer import check_tensor
-
 CPU = torch.device("cpu")
 
 
-def test_a_matching_tensor_passes():
+@pytest.fixture(scope="module")
+def check_tensor():
+    from combine_ep_layout_04_gb300 import build
+    build.build()                      # the binding loads libep.so on import
+    from combine_ep_layout_04_gb300.layer import check_tensor
+    return check_tensor
+
+
+def test_a_matching_tensor_passes(check_tensor):
     check_tensor(torch.zeros(4, 3, dtype=torch.int32), "t", torch.int32, CPU, (4, 3))
     check_tensor(torch.zeros(7, 3, dtype=torch.int32), "t", torch.int32, CPU, (None, 3))
 
@@ -22,11 +28,11 @@ def test_a_matching_tensor_passes():
     (torch.zeros(4, 3, 1, dtype=torch.int32), ValueError),         # rank
     ([[0] * 3] * 4, TypeError),                                    # not a tensor
 ])
-def test_a_wrong_tensor_is_refused(t, exc):
+def test_a_wrong_tensor_is_refused(check_tensor, t, exc):
     with pytest.raises(exc):
         check_tensor(t, "t", torch.int32, CPU, (4, 3))
 
 
-def test_a_tensor_on_another_device_is_refused():
+def test_a_tensor_on_another_device_is_refused(check_tensor):
     with pytest.raises(ValueError, match="on cpu"):
         check_tensor(torch.zeros(4, 3, dtype=torch.int32), "t", torch.int32, torch.device("cuda", 0), (4, 3))
