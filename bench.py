@@ -153,57 +153,116 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle
-def cpu_oracle_rates(w, idx, wt, x_dev, eo_dev, budget_s: float = 12.0):
-    """Time the oracle (single thread) on a bounded sample of the workload:
-    the full layout, the dispatch of one source rank's tokens, and the combine
-    of a token sample.  Returns per-op GB/s of algorithmic bytes and a note."""
+def cpu_info() -> dict:
+    """Host cores and CPU model of the machine the oracle is timed on."""
+    import platform
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    return {"nproc": os.cpu_count(), "cpu_model": model or platform.processor() or "unknown",
+            "arch": platform.machine()}
+
+
+class OracleSample:
+    """A bounded sample of one step for the single-threaded CPU oracle: the
+    whole layout, then the dispatch and the combine of the tokens of source
+    ranks [0, s_end), s_end = max(1, round(R * frac)).  With frac = 1 it is the
+    whole step.  x_rows(t1) gives the bf16 bits of tokens [0, t1); eo_rows(rows)
+    the bf16 bits of the given expert-output rows (sorted); both are fetched
+    once, outside any timing.  The combine reads only the rows its tokens
+    need, renumbered into a compact array (each token's rows keep their
+    meaning)."""
+
+    def __init__(self, w, idx, wt, x_rows, eo_rows, frac: float):
+        import oracle
+        self.w = w
+        R, Tpr, H, E, K = w.num_ranks, w.tokens_per_rank, w.hidden, w.num_experts, w.topk
+        B = 2 * H
+        self.G = w.rows_per_msg or oracle.default_rows_per_msg(H)
+        self.idx = np.ascontiguousarray(idx)
+        lay = oracle.layout(R, Tpr, E, self.idx, self.G)
+        self.s_end = max(1, min(R, int(round(R * frac))))
+        t1 = self.s_end * Tpr
+        self.t1 = t1
+        self.frac = self.s_end / R
+        ts = lay["token_slot"][:t1]
+        mask = ts >= 0
+        rows = lay["recv_base"].astype(np.int64)[None, :] + ts
+        uniq = np.unique(rows[mask])
+        self.sub_lay = {"token_slot": np.ascontiguousarray(np.where(mask, np.searchsorted(uniq, rows), -1)
+                                                           .astype(np.int32)),
+                        "recv_base": np.zeros(R, np.int32)}
+        self.idx_s = np.ascontiguousarray(self.idx[:t1])
+        self.wt_s = np.ascontiguousarray(wt[:t1])
+        self.xs = np.ascontiguousarray(x_rows(t1))
+        self.eo = np.ascontiguousarray(eo_rows(uniq)) if len(uniq) else np.zeros((1, H), np.uint16)
+        self.recv = np.empty((lay["n_recv"], H), np.uint16)   # pages touched only where written
+        n_rows = int(mask.sum())
+        sent = int(mask.any(axis=1).sum())
+        msgs = int(lay["msg_count"][:self.s_end].sum())
+        full = algorithmic_bytes(R, w.num_tokens, H, E, K, lay["n_recv"], int(lay["msg_count"].sum()),
+                                 int(lay["is_token_in_rank"].any(axis=1).sum()))
+        self.bytes = {"layout": full["layout"],
+                      "dispatch": sent * B + n_rows * B + t1 * R * 4 + msgs * 32,
+                      "combine": n_rows * B + t1 * B + t1 * K * 8 + t1 * R * 4}
+        self.desc = (f"whole layout; dispatch and combine of the tokens of source ranks [0, {self.s_end}) of "
+                     f"{R} ({t1} of {w.num_tokens} tokens, fraction {self.frac:g})")
+
+    def run(self) -> dict:
+        """One pass; seconds per op."""
+        import oracle
+        w = self.w
+        c0 = time.perf_counter()
+        lay = oracle.layout(w.num_ranks, w.tokens_per_rank, w.num_experts, self.idx, self.G)
+        c1 = time.perf_counter()
+        oracle.dispatch(lay, self.xs, 0, self.t1, recv=self.recv, x_first_token=0)
+        c2 = time.perf_counter()
+        oracle.combine(self.sub_lay, self.idx_s, self.wt_s, w.experts_per_rank, self.eo)
+        c3 = time.perf_counter()
+        return {"layout": c1 - c0, "dispatch": c2 - c1, "combine": c3 - c2}
+
+    def measure(self, runs: int = 3) -> dict:
+        """Median of `runs` passes: per-op seconds and GB/s, and GB/s over the
+        sample."""
+        ts = [self.run() for _ in range(runs)]
+        med = {k: float(np.median([t[k] for t in ts])) for k in ts[0]}
+        tot = sum(med.values())
+        return {"value": round(sum(self.bytes.values()) / tot / 1e9, 3), "unit": "GB/s",
+                "seconds_per_sample": round(tot, 4), "runs": runs,
+                "per_op_GBps": {k: round(self.bytes[k] / med[k] / 1e9, 3) for k in med},
+                "per_op_s": {k: round(med[k], 5) for k in med}, "sample": self.desc}
+
+
+def oracle_sample_from_device(w, idx, wt, x_dev, eo_dev, frac):
+    """OracleSample whose inputs are the bench's own device tensors."""
     import torch
 
-    import oracle
-    R, Tpr, H, E, K = w.num_ranks, w.tokens_per_rank, w.hidden, w.num_experts, w.topk
-    T, B = w.num_tokens, 2 * w.hidden
-    G = oracle.default_rows_per_msg(H)
-    t0 = time.perf_counter()
-    lay = oracle.layout(R, Tpr, E, idx, G)
-    t_layout = time.perf_counter() - t0
-    N = lay["n_recv"]
-    n_msgs = int(lay["msg_count"].sum())
-    full = algorithmic_bytes(R, T, H, E, K, N, n_msgs, T)
-    rates = {"layout": full["layout"] / t_layout / 1e9}
-    # dispatch: source ranks' tokens until about a third of the budget
-    recv = np.empty((N, H), np.uint16)
-    done_tok, t_disp, bytes_disp = 0, 0.0, 0
-    while done_tok < T and t_disp < budget_s / 3:
-        t1 = min(T, done_tok + Tpr)
-        xs = x_dev[done_tok:t1].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-        c0 = time.perf_counter()
-        oracle.dispatch(lay, xs, done_tok, t1, recv=recv, x_first_token=done_tok)
-        t_disp += time.perf_counter() - c0
-        rows = int((lay["token_slot"][done_tok:t1] >= 0).sum())
-        bytes_disp += (t1 - done_tok) * B + rows * B + (t1 - done_tok) * R * 4 + rows // G * 32
-        done_tok = t1
-    rates["dispatch"] = bytes_disp / t_disp / 1e9
-    # combine: a token sample, reading only the rows it needs
-    ntok = max(16, min(256, int(256 * budget_s / 12.0))) if budget_s < 12.0 else 256
-    rng = np.random.default_rng(0)
-    toks = np.sort(rng.choice(T, min(T, ntok), replace=False))
-    need = sorted({int(lay["recv_base"][d]) + int(lay["token_slot"][t, d])
-                   for t in toks for d in range(R) if lay["token_slot"][t, d] >= 0})
-    eo = eo_dev.index_select(0, torch.tensor(need, device=eo_dev.device)).view(torch.int16).cpu().numpy().view(np.uint16)
-    pos = {r: i for i, r in enumerate(need)}
-    sub = np.full((len(toks), R), -1, np.int32)
-    for i, t in enumerate(toks):
-        for d in range(R):
-            if lay["token_slot"][t, d] >= 0:
-                sub[i, d] = pos[int(lay["recv_base"][d]) + int(lay["token_slot"][t, d])]
-    c0 = time.perf_counter()
-    oracle.combine({"token_slot": sub, "recv_base": np.zeros(R, np.int32)}, idx[toks], wt[toks], E // R, eo)
-    t_comb = time.perf_counter() - c0
-    bytes_comb = len(need) * B + len(toks) * B + len(toks) * K * 8 + len(toks) * R * 4
-    rates["combine"] = bytes_comb / t_comb / 1e9
-    note = (f"oracle, 1 thread: full layout; dispatch of {done_tok} tokens ({done_tok // Tpr} source ranks); "
-            f"combine of {len(toks)} tokens; GB/s per op scaled to the full step")
-    return rates, full, note
+    def x_rows(t1):
+        return x_dev[:t1].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+    def eo_rows(rows):
+        r = torch.from_numpy(rows).to(eo_dev.device)
+        return eo_dev.index_select(0, r).view(torch.int16).cpu().numpy().view(np.uint16)
+
+    return OracleSample(w, idx, wt, x_rows, eo_rows, frac)
+
+
+def oracle_sample_on_host(w, idx, wt, frac):
+    """OracleSample whose inputs are drawn on the host (no GPU involved)."""
+    import workloads as W
+    return OracleSample(w, idx, wt, lambda t1: W.make_x(w, rows=t1),
+                        lambda rows: W.make_expert_out(len(rows), w.hidden, w.seed), frac)
+
+
+# fraction of each workload's step the CPU oracle is timed on: the whole step
+# for the small layers, a fixed share of the source ranks for the large ones
+CPU_FRACTION = {"tiny": 1.0, "ll": 1.0, "small": 1.0, "skew": 0.25, "ht": 0.25}
 
 
 def slowest_rank(step_s: float, dist, device) -> float:
@@ -221,12 +280,6 @@ def job_gbps(world: int, bytes_per_replica: int, step_s: float) -> float:
     """Whole-job GB/s: every replica moves the same bytes per step, and the
     job's step lasts as long as its slowest replica's."""
     return world * bytes_per_replica / step_s / 1e9
-
-
-def step_rate(full: dict, rates: dict) -> tuple[float, float]:
-    """(GB/s over the whole step, seconds per step) at the given per-op rates."""
-    secs = sum(full[k] / (rates[k] * 1e9) for k in full)
-    return sum(full.values()) / secs / 1e9, secs
 
 
 # ---------------------------------------------------------------------- main
@@ -275,76 +328,30 @@ def main():
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
         dist.init_process_group("nccl", device_id=dev)
 
-    from combine_ep_layout_04_gb300 import EpLayer
-
-    R, Tpr, H, E, K = w.num_ranks, w.tokens_per_rank, w.hidden, w.num_experts, w.topk
-    T = w.num_tokens
-    idx, wt = W.make_routing(w)
-    x = W.make_x_torch(w, dev)
-    topk = torch.from_numpy(idx).to(dev)
-    wts = torch.from_numpy(wt).to(dev)
-    layer = EpLayer(R, Tpr, H, E, K, channels=w.channels, ring_depth=w.ring_depth, max_inflight=w.max_inflight,
-                    rows_per_msg=w.rows_per_msg, device=dev)
-    lay = layer.layout(topk)            # sizes recv once; every step recomputes the layout
-    N = lay.n_recv
-    recv = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
-    eo = W.make_expert_out_torch(N, H, dev, w.seed)
-    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-    n_msgs = int(lay.msg_count.sum())
-    n_sent = int((lay.is_token_in_rank.sum(dim=1) > 0).sum())
-    ab = algorithmic_bytes(R, T, H, E, K, N, n_msgs, n_sent)
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or 128 * 2**20
     flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
-    st = torch.cuda.current_stream(dev)
+    peak, peak_kind = read_peaks()
 
-    def step():
-        layer.layout(topk, out=lay, sync=False)
-        layer.dispatch(x, lay, recv)
-        layer.combine(eo, wts, topk, lay, out)
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize(dev)
-    if layer.device_status() != 0:
-        raise SystemExit(f"device status {layer.device_status()} after warm-up")
-
+    case = GpuCase(w, dev, flush)
+    case.warm(args.warmup)
     clocks = ClockSampler(local)
     time.sleep(0.6)
     K_ = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K_)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
     wall0 = time.time()
-    for i in range(K_):
-        flush.zero_()
-        e = evs[i]
-        e[0].record(st)
-        layer.layout(topk, out=lay, sync=False)
-        e[1].record(st)
-        layer.dispatch(x, lay, recv)
-        e[2].record(st)
-        layer.combine(eo, wts, topk, lay, out)
-        e[3].record(st)
-    torch.cuda.synchronize(dev)
+    t_layout, t_disp, t_comb = case.timed_steps(K_)
     if dist:
         dist.barrier()
     wall1 = time.time()
-    clocks.stop()
-    status = layer.device_status()
-    if status != 0:
-        raise SystemExit(f"device status {status} in the timed region")
-    t_layout = np.array([e[0].elapsed_time(e[1]) for e in evs]) * 1e-3
-    t_disp = np.array([e[1].elapsed_time(e[2]) for e in evs]) * 1e-3
-    t_comb = np.array([e[2].elapsed_time(e[3]) for e in evs]) * 1e-3
     t_step = t_layout + t_disp + t_comb
     step_s = slowest_rank(float(t_step.mean()), dist, dev)
+    ab = case.ab
     total_bytes = sum(ab.values())
     value = job_gbps(world, total_bytes, step_s)
 
-    peak, peak_kind = read_peaks()
     per_op = {"layout": float(t_layout.mean()), "dispatch": float(t_disp.mean()), "combine": float(t_comb.mean())}
     dom = max(("dispatch", "combine"), key=lambda k: per_op[k])
     achieved = ab[dom] / per_op[dom] / 1e9
@@ -355,43 +362,168 @@ def main():
                 "per_op": {k: {"us": round(per_op[k] * 1e6, 2), "bytes": ab[k],
                                "GBps": round(ab[k] / per_op[k] / 1e9, 1),
                                "frac": round(ab[k] / per_op[k] / 1e9 / peak, 4)} for k in per_op}}
-
+    T, H, R, E, K = w.num_tokens, w.hidden, w.num_ranks, w.num_experts, w.topk
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K_,
         "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT[args.workload] + (
-                       f" (tokens per rank {Tpr})" if args.tokens_per_rank else ""), "name": w.name, "num_tokens": T,
-                   "hidden": H, "ranks": R, "experts": E, "topk": K, "n_recv": N, "messages": n_msgs,
-                   "rows_per_msg": layer.G, "l2": "flushed between steps (write of 2x L2, outside the events)",
+                       f" (tokens per rank {w.tokens_per_rank})" if args.tokens_per_rank else ""), "name": w.name,
+                   "num_tokens": T, "hidden": H, "ranks": R, "experts": E, "topk": K, "n_recv": case.N,
+                   "messages": case.n_msgs, "rows_per_msg": case.layer.G,
+                   "l2": "flushed between steps (write of 2x L2, outside the events)",
                    "parallelism": "replicas" if world > 1 else "1 GPU"},
         "us_per_layer": round((per_op["dispatch"] + per_op["combine"]) * 1e6, 2),
         "dispatch_us": round(per_op["dispatch"] * 1e6, 2), "combine_us": round(per_op["combine"] * 1e6, 2),
         "layout_us": round(per_op["layout"] * 1e6, 2),
         "roofline": roofline,
         "gpu_launches": 3 * K_,
-        "clocks": clocks.summary(wall0, wall1),
+        "clocks": None,
         "wall_s_timed_region": round(wall1 - wall0, 3),
     }
 
-    result["next_rows"] = {"expert_layout": time_expert_layout(layer, topk, wts, lay, flush, st, peak, w, N)}
+    result["next_rows"] = {"expert_layout": time_expert_layout(case, peak)}
     if not args.no_e2e:
-        result["e2e"] = run_e2e(layer, w, idx, wt, x, lay, recv, out, ab, dev, K_=max(3, min(K_, 10)))
+        result["e2e"] = run_e2e(case, dev, K_=max(3, min(K_, 10)))
+    cpu_case = None
     if rank == 0 and not args.no_cpu_baseline and world == 1:
-        rates, full, note = cpu_oracle_rates(w, idx, wt, x, eo)
-        v, secs = step_rate(full, rates)
-        result["cpu_baseline"] = {"value": round(v, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                  "sample": note, "per_op_GBps": {k: round(r, 3) for k, r in rates.items()}}
-    layer.close()
+        cpu_case = oracle_sample_from_device(w, case.idx, case.wt, case.x, case.eo,
+                                             CPU_FRACTION.get(args.workload, 1.0) if not args.tokens_per_rank
+                                             else 1.0)
+    case.close()
+    del case
+
+    # every workload, timed the same way (the headline above is the default one)
+    if not args.tokens_per_rank:
+        per_config = {}
+        for name in ("tiny", "ll", "ht", "skew", "small"):
+            if name == args.workload:
+                per_config[name] = {"steps": K_, "n_recv": result["config"]["n_recv"],
+                                    **{f"{k}_us": roofline["per_op"][k]["us"] for k in per_op},
+                                    "per_op": roofline["per_op"]}
+                continue
+            wc = W.get(name)
+            c = GpuCase(wc, dev, flush)
+            c.warm(args.warmup)
+            tl, td, tc = c.timed_steps(max(20, K_))
+            per_config[name] = c.summary(tl, td, tc, peak)
+            c.close()
+            del c
+        result["per_config"] = per_config
+    clocks.stop()
+    result["clocks"] = clocks.summary(wall0, wall1)
+    result["clocks_whole_run"] = clocks.summary(wall0 - 1.0, time.time())
+
+    if cpu_case is not None:
+        meas = cpu_case.measure(runs=3)
+        info = cpu_info()
+        result["cpu_baseline"] = {"value": meas["value"], "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                  "sample": f"oracle (gcc -O3, 1 thread), median of {meas['runs']} runs: "
+                                            + meas["sample"],
+                                  "per_op_GBps": meas["per_op_GBps"], "seconds_per_sample": meas["seconds_per_sample"],
+                                  **info}
+        if not args.tokens_per_rank:
+            per = {}
+            for name in ("tiny", "ll", "skew", "small"):
+                if name == args.workload:
+                    continue
+                wc = W.get(name)
+                idx_c, wt_c = W.make_routing(wc)
+                m = oracle_sample_on_host(wc, idx_c, wt_c, CPU_FRACTION[name]).measure(runs=3)
+                per[name] = {k: m[k] for k in ("value", "per_op_GBps", "seconds_per_sample", "sample")}
+            result["cpu_baseline"]["per_config"] = per
     if rank == 0:
         print(json.dumps(result))
     if dist:
         dist.destroy_process_group()
 
-def time_expert_layout(layer, topk, wts, lay, flush, st, peak, w, N, reps: int = 20):
+
+class GpuCase:
+    """One workload resident on the GPU: inputs, a handle, the layout, the
+    receive buffer, a random expert output and the combine output.  A step is
+    ep_layout (not waiting for N), ep_dispatch and ep_combine on the current
+    stream; the L2 is flushed before each step, outside the events."""
+
+    def __init__(self, w, dev, flush):
+        import torch
+
+        import workloads as W
+        from combine_ep_layout_04_gb300 import EpLayer
+        self.w, self.dev, self.flush = w, dev, flush
+        R, Tpr, H, E, K = w.num_ranks, w.tokens_per_rank, w.hidden, w.num_experts, w.topk
+        self.idx, self.wt = W.make_routing(w)
+        self.x = W.make_x_torch(w, dev)
+        self.topk = torch.from_numpy(self.idx).to(dev)
+        self.wts = torch.from_numpy(self.wt).to(dev)
+        self.layer = EpLayer(R, Tpr, H, E, K, channels=w.channels, ring_depth=w.ring_depth,
+                             max_inflight=w.max_inflight, rows_per_msg=w.rows_per_msg, device=dev)
+        self.lay = self.layer.layout(self.topk)   # sizes recv once; every step recomputes the layout
+        self.N = self.lay.n_recv
+        self.recv = torch.empty((self.N, H), dtype=torch.bfloat16, device=dev)
+        self.eo = W.make_expert_out_torch(self.N, H, dev, w.seed)
+        self.out = torch.empty((w.num_tokens, H), dtype=torch.bfloat16, device=dev)
+        self.n_msgs = int(self.lay.msg_count.sum())
+        n_sent = int((self.lay.is_token_in_rank.sum(dim=1) > 0).sum())
+        self.ab = algorithmic_bytes(R, w.num_tokens, H, E, K, self.N, self.n_msgs, n_sent)
+        self.st = torch.cuda.current_stream(dev)
+
+    def step(self):
+        self.layer.layout(self.topk, out=self.lay, sync=False)
+        self.layer.dispatch(self.x, self.lay, self.recv)
+        self.layer.combine(self.eo, self.wts, self.topk, self.lay, self.out)
+
+    def warm(self, n):
+        import torch
+        for _ in range(n):
+            self.flush.zero_()
+            self.step()
+        torch.cuda.synchronize(self.dev)
+        if self.layer.device_status() != 0:
+            raise SystemExit(f"device status {self.layer.device_status()} after warm-up ({self.w.name})")
+
+    def timed_steps(self, n):
+        """Seconds of layout, dispatch and combine in each of n steps (CUDA
+        events on the launching stream)."""
+        import torch
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+        torch.cuda.synchronize(self.dev)
+        for i in range(n):
+            self.flush.zero_()
+            e = evs[i]
+            e[0].record(self.st)
+            self.layer.layout(self.topk, out=self.lay, sync=False)
+            e[1].record(self.st)
+            self.layer.dispatch(self.x, self.lay, self.recv)
+            e[2].record(self.st)
+            self.layer.combine(self.eo, self.wts, self.topk, self.lay, self.out)
+            e[3].record(self.st)
+        torch.cuda.synchronize(self.dev)
+        status = self.layer.device_status()
+        if status != 0:
+            raise SystemExit(f"device status {status} in the timed region ({self.w.name})")
+        return tuple(np.array([e[j].elapsed_time(e[j + 1]) for e in evs]) * 1e-3 for j in range(3))
+
+    def summary(self, tl, td, tc, peak):
+        out = {"steps": len(tl), "n_recv": self.N, "messages": self.n_msgs, "per_op": {}}
+        for k, t in (("layout", tl), ("dispatch", td), ("combine", tc)):
+            m = float(t.mean())
+            out[f"{k}_us"] = round(m * 1e6, 2)
+            out["per_op"][k] = {"us": round(m * 1e6, 2), "us_median": round(float(np.median(t)) * 1e6, 2),
+                                "bytes": self.ab[k], "GBps": round(self.ab[k] / m / 1e9, 1),
+                                "frac": round(self.ab[k] / m / 1e9 / peak, 4)}
+        return out
+
+    def close(self):
+        self.layer.close()
+        self.x = self.recv = self.eo = self.out = self.topk = self.wts = None
+
+
+def time_expert_layout(case, peak, reps: int = 20):
     """ep_expert_layout timed on its own (it is not part of the step): median
     of `reps` launches with the L2 flushed before each."""
     import torch
+    layer, topk, wts, lay, flush, st, w, N = (case.layer, case.topk, case.wts, case.lay, case.flush, case.st,
+                                              case.w, case.N)
     lay.n_recv = N            # the step's layouts ran without waiting for N
     xl = layer.expert_layout(topk, wts, lay)
     T, K, E = w.num_tokens, w.topk, w.num_experts
@@ -648,7 +780,7 @@ def run_sweep(args):
         del x, topk
 
 
-def run_e2e(layer, w, idx, wt, x_dev, lay, recv, out, ab, dev, K_):
+def run_e2e(case, dev, K_):
     """The same step through the public API with host buffers.  Every step
     copies its x, topk_idx and topk_weights from pinned host memory to the
     device, runs layout, dispatch, the identity expert (combine reads the
@@ -659,6 +791,8 @@ def run_e2e(layer, w, idx, wt, x_dev, lay, recv, out, ab, dev, K_):
     each way) while step i computes; inputs and outputs are double-buffered,
     and events order every reuse of a buffer."""
     import torch
+    layer, w, idx, wt, x_dev, lay, recv, out, ab = (case.layer, case.w, case.idx, case.wt, case.x, case.lay,
+                                                    case.recv, case.out, case.ab)
     T, H, K = w.num_tokens, w.hidden, w.topk
     x_h = x_dev.cpu().pin_memory()
     idx_h = torch.from_numpy(idx).pin_memory()
@@ -725,56 +859,43 @@ def run_e2e(layer, w, idx, wt, x_dev, lay, recv, out, ab, dev, K_):
 
 
 def run_reference(args, w, world, rank):
-    """The CPU oracle, as it stands, on the host cores: each step a bounded
-    sample of the same workload; same metric and unit."""
+    """The CPU oracle, as it stands, on the host cores (one thread): each step
+    is one pass over the same bounded sample of the workload -- the whole
+    layout, then the dispatch and combine of a fixed share of the source
+    ranks (CPU_FRACTION) -- with its inputs drawn on the host beforehand.
+    value = the sample's algorithmic bytes / the measured seconds, and
+    ms_per_step is the measured time of one pass, so steps x ms_per_step is
+    the timed region.  Same metric and unit as the GPU arm."""
     if rank != 0:
         return
-    import torch
-
     import workloads as W
     idx, wt = W.make_routing(w)
-    x = W.make_x_torch(w, "cpu")
-    eo_rows = None
-    import oracle
-    lay = oracle.layout(w.num_ranks, w.tokens_per_rank, w.num_experts, idx, oracle.default_rows_per_msg(w.hidden))
-    eo_rows = lay["n_recv"]
-    # expert output: only the sampled rows are read; draw it lazily by rows
-    eo = _LazyRows(eo_rows, w.hidden, w.seed)
-    vals = []
-    # each step a bounded sample, sized so that the whole run stays within a
-    # couple of minutes whatever --steps is
-    budget = max(0.1, min(1.0, 90.0 / (args.warmup + args.steps)))
-    for i in range(args.warmup + args.steps):
-        rates, full, note = cpu_oracle_rates(w, idx, wt, x, eo, budget_s=budget)
-        v, secs = step_rate(full, rates)
-        if i >= args.warmup:
-            vals.append((v, secs))
-    v = float(np.mean([a for a, _ in vals]))
-    secs = float(np.mean([b for _, b in vals]))
+    frac = CPU_FRACTION.get(args.workload, 1.0) if not args.tokens_per_rank else 1.0
+    if args.workload == "ht" and not args.tokens_per_rank:
+        frac = 0.125     # keeps a 25-step run within about half a minute
+    sample = oracle_sample_on_host(w, idx, wt, frac)
+    for _ in range(args.warmup):
+        sample.run()
+    t0 = time.perf_counter()
+    per = [sample.run() for _ in range(args.steps)]
+    wall = time.perf_counter() - t0
+    secs = wall / args.steps
+    nbytes = sum(sample.bytes.values())
+    v = nbytes / secs / 1e9
+    info = cpu_info()
+    note = f"oracle (gcc -O3, 1 thread), one pass per step: {sample.desc}"
     res = {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "GB/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3, 3),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-           "data": "synthetic", "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload},
-           "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": note},
-           "e2e": {"value": round(v, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+           "data": "synthetic",
+           "config": {"workload": WORKLOAD_TEXT[args.workload], "name": w.name,
+                      "sample_fraction_of_step": sample.frac, "bytes_per_sample": nbytes},
+           "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": note,
+                            "per_op_GBps": {k: round(sample.bytes[k] / float(np.median([p[k] for p in per])) / 1e9, 3)
+                                            for k in sample.bytes}, **info},
+           "e2e": {"value": round(v, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+           "wall_s_timed_region": round(wall, 3)}
     print(json.dumps(res))
-
-
-class _LazyRows:
-    """Expert output rows drawn on demand (row r from a seed of its own), so
-    that the CPU reference never materialises the whole [N, H] array."""
-
-    def __init__(self, rows, hidden, seed):
-        self.rows, self.hidden, self.seed = rows, hidden, seed
-        self.device = "cpu"
-
-    def index_select(self, dim, index):
-        import torch
-        out = torch.empty((len(index), self.hidden), dtype=torch.bfloat16)
-        for i, r in enumerate(index.tolist()):
-            g = torch.Generator().manual_seed(self.seed * 1000003 + r)
-            out[i] = torch.randn(self.hidden, generator=g)
-        return out
 
 
 if __name__ == "__main__":

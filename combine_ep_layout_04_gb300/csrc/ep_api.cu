@@ -31,16 +31,18 @@ bool ptr_usable_on(int device, const void *p) {
     }
 }
 
+// Rows per message: 8 when a bf16 row is under the 7 KB packing threshold
+// (UCCL-EP article s4.1; batch size 8 from s5.3), else 1.
+int default_rows_per_msg(int hidden) { return 2 * hidden < 7 * 1024 ? 8 : 1; }
+
 }  // namespace ep
+
+using ep::default_rows_per_msg;
 
 namespace {
 
 bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-// Rows per message: 8 when a bf16 row is under the 7 KB packing threshold
-// (UCCL-EP article s4.1; batch size 8 from s5.3), else 1.
-int default_rows_per_msg(int hidden) { return 2 * hidden < 7 * 1024 ? 8 : 1; }
 
 ep_status cuda_ok(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
 

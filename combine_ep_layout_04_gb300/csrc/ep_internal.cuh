@@ -155,6 +155,8 @@ ep_status launch_wait_signal(const unsigned long long *signal, unsigned long lon
 ep_status launch_expert_layout(ep_ctx *h, const int32_t *topk_idx, const float *topk_weights,
                                const ep_layout_out *lay, const ep_expert_layout_out *out,
                                int64_t recv_rows, int64_t rows_cap, cudaStream_t st);
+// Rows per message G when ep_config.rows_per_msg is 0 (ep_api.cu).
+int default_rows_per_msg(int hidden);
 // Dispatch geometry, decided once per handle.
 ep_status plan_dispatch(ep_ctx *h);
 ep_status plan_combine(ep_ctx *h);

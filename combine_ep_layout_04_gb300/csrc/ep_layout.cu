@@ -433,7 +433,7 @@ extern "C" ep_status ep_layout_static(const ep_config *cfg, const int32_t *topk_
     p.E = cfg->num_experts;
     p.K = cfg->topk;
     p.Er = p.E / p.R;
-    p.G = cfg->rows_per_msg ? cfg->rows_per_msg : (2 * cfg->hidden < 7 * 1024 ? 8 : 1);
+    p.G = cfg->rows_per_msg ? cfg->rows_per_msg : default_rows_per_msg(cfg->hidden);
     p.tiles = static_cast<int>((T + 255) / 256);
     p.dev.err = reinterpret_cast<int32_t *>(b + kSErr);
     p.dev.ticket = reinterpret_cast<unsigned long long *>(b + kSTicket);

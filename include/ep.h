@@ -387,9 +387,14 @@ ep_status ep_get_info(ep_handle h, ep_info *out);
  *  n_recv_host: if non-NULL, the call synchronises `stream`, writes N and
  *               returns the device-side status of this call (EP_ERR_INVALID_ARG
  *               for a pick outside [-1, E)); if NULL it returns without waiting
- *               and device-side errors are not reported.
+ *               and device-side errors are not reported: the next call clears
+ *               the array's error word before it starts, so a caller that
+ *               never waits for N must validate topk_idx itself (every pick in
+ *               [-1, E)) or check the outputs by other means.
  * The first call on a device looks up the array's device address (once per
- * device, under a lock); make that first call before any stream capture.
+ * device, under a lock) and keeps it for the life of the process; make that
+ * first call before any stream capture.  cudaDeviceReset on a device after
+ * its first call is not supported: the address kept would then be stale.
  * Every call on a device shares the one array and the call clears the parts
  * it needs at zero first, so calls must not overlap on the GPU: two calls in
  * flight at once (on different streams, or from different threads) race. */

@@ -49,12 +49,14 @@ def default_rows_per_msg(hidden: int) -> int:
 
 
 def build(force: bool = False) -> str:
-    """Compile ep_oracle.c into liboracle.so next to it (gcc, -O2, no FMA
-    contraction so every fused multiply-add is the explicit fmaf)."""
+    """Compile ep_oracle.c into liboracle.so next to it (gcc -O3, no FMA
+    contraction and no fast-math, so every fused multiply-add is the explicit
+    fmaf and every other operation is rounded as written; no -march=native,
+    so the x86 and Arm builds give the same results)."""
     if force or not os.path.exists(_LIB_PATH) or \
             os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+        subprocess.run(["gcc", "-O3", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
                         "-fno-fast-math", "-o", tmp, _SRC, "-lm"], check=True)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH

@@ -77,26 +77,103 @@ def check_dispatch_rows(recv: torch.Tensor, x: torch.Tensor, lay_o: dict, chunk_
 
 def oracle_combine_sample(lay_o: dict, idx: np.ndarray, wt: np.ndarray, Er: int, expert_out: torch.Tensor,
                           tokens: np.ndarray) -> np.ndarray:
-    """Oracle combine for a sample of tokens, fetching only the expert_out rows
+    """Oracle combine for a set of tokens, fetching only the expert_out rows
     those tokens read (the receive rows are renumbered into a compact array;
     row(t, k) is unchanged in meaning)."""
+    tokens = np.asarray(tokens, dtype=np.int64)
     R = lay_o["recv_base"].shape[0]
-    need = []
-    for t in tokens:
-        for d in range(R):
-            if lay_o["token_slot"][t, d] >= 0:
-                need.append(int(lay_o["recv_base"][d]) + int(lay_o["token_slot"][t, d]))
-    uniq = np.array(sorted(set(need)), dtype=np.int64)
+    ts = lay_o["token_slot"][tokens]
+    mask = ts >= 0
+    rows = lay_o["recv_base"].astype(np.int64)[None, :] + ts
+    uniq = np.unique(rows[mask])
     eo = bf16_tensor_to_bits(expert_out.index_select(0, torch.from_numpy(uniq).to(expert_out.device))) \
         if len(uniq) else np.zeros((1, expert_out.shape[1]), np.uint16)
-    pos = {int(r): i for i, r in enumerate(uniq)}
-    sub_slot = np.full((len(tokens), R), -1, np.int32)
-    for i, t in enumerate(tokens):
-        for d in range(R):
-            if lay_o["token_slot"][t, d] >= 0:
-                sub_slot[i, d] = pos[int(lay_o["recv_base"][d]) + int(lay_o["token_slot"][t, d])]
-    sub_lay = {"token_slot": sub_slot, "recv_base": np.zeros(R, np.int32)}
+    sub_slot = np.where(mask, np.searchsorted(uniq, rows), -1).astype(np.int32)
+    sub_lay = {"token_slot": np.ascontiguousarray(sub_slot), "recv_base": np.zeros(R, np.int32)}
     return oracle.combine(sub_lay, idx[tokens], wt[tokens], Er, eo)
+
+
+def check_combine_all(out: torch.Tensor, lay_o: dict, idx: np.ndarray, wt: np.ndarray, Er: int,
+                      expert_out: torch.Tensor, max_ulp: int, chunk: int = 8192, workers: int = 0) -> int:
+    """Every element of `out` against the oracle's combine, token chunk by
+    token chunk so that host memory stays bounded; the oracle runs on a pool
+    of host threads (it is single-threaded C called through ctypes, which
+    releases the GIL).  Raises on the first element more than max_ulp bf16
+    ulps away; returns the largest distance seen."""
+    import concurrent.futures as cf
+    import os
+    T = idx.shape[0]
+    workers = workers or max(1, min(8, (os.cpu_count() or 2) - 1))
+    worst = 0
+
+    def finish(fut):
+        nonlocal worst
+        t0, got, ref = fut.result()
+        ulp = bf16_ulp_distance(got, ref)
+        m = int(ulp.max(initial=0))
+        if m > max_ulp:
+            bad = np.argwhere(ulp > max_ulp)[:5]
+            raise AssertionError(f"combine: max ulp {m}; first elements (token, column) "
+                                 f"{[(int(t0 + b[0]), int(b[1])) for b in bad]}")
+        worst = max(worst, m)
+
+    def job(t0, tokens, got, rows):
+        return t0, got, oracle_combine_sample(lay_o, idx, wt, Er, rows, tokens)
+
+    # expert_out rows are gathered on the device in the main thread (torch
+    # calls stay on one thread); only the oracle runs in the pool, with at
+    # most 2 * workers chunks held on the host
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        pending = []
+        for t0 in range(0, T, chunk):
+            t1 = min(T, t0 + chunk)
+            tokens = np.arange(t0, t1)
+            ts = lay_o["token_slot"][t0:t1]
+            mask = ts >= 0
+            rows = lay_o["recv_base"].astype(np.int64)[None, :] + ts
+            uniq = np.unique(rows[mask])
+            got = bf16_tensor_to_bits(out[t0:t1])
+            pending.append(ex.submit(job, t0, tokens, got, _HostRows(expert_out, uniq)))
+            while len(pending) >= 2 * workers:
+                finish(pending.pop(0))
+        for f in pending:
+            finish(f)
+    return worst
+
+
+class _HostRows:
+    """The rows `uniq` of a device tensor, copied to the host once, served to
+    oracle_combine_sample's index_select (which asks for exactly those rows,
+    in the same sorted order)."""
+
+    def __init__(self, t: torch.Tensor, uniq: np.ndarray):
+        self.shape = t.shape
+        self.device = "cpu"
+        self._uniq = uniq
+        self._rows = t.index_select(0, torch.from_numpy(uniq).to(t.device)).cpu() if len(uniq) else None
+
+    def index_select(self, dim, index):
+        assert dim == 0 and np.array_equal(index.cpu().numpy(), self._uniq)
+        return self._rows
+
+
+def check_identity_all(out_id: torch.Tensor, x: torch.Tensor, wt: np.ndarray, topk: int,
+                       chunk: int = 8192) -> None:
+    """dispatch -> identity expert -> combine == x * sum_k w on every token,
+    within one bf16 rounding plus the fp32 chain's reassociation error
+    (tokens with no picks combine to zero)."""
+    T = x.shape[0]
+    for t0 in range(0, T, chunk):
+        t1 = min(T, t0 + chunk)
+        xf = x[t0:t1].double()
+        sw = torch.from_numpy(wt[t0:t1].astype(np.float64)).to(x.device).sum(dim=1, keepdim=True)
+        ref = xf * sw
+        err = (out_id[t0:t1].double() - ref).abs()
+        bound = ref.abs() * 2.0**-8 + topk * 2.0**-23 * xf.abs() * sw + 1e-30
+        if not bool((err <= bound).all()):
+            bad = (err > bound).nonzero()[:5].tolist()
+            raise AssertionError(f"identity-expert combine off at (token, column) "
+                                 f"{[(t0 + b[0], b[1]) for b in bad]}")
 
 
 def check_ring_invariants(layer, logs, lay_o, before=None) -> None:

@@ -27,7 +27,7 @@ import dataclasses
 import numpy as np
 
 __all__ = ["Workload", "WORKLOADS", "get", "make_routing", "make_x", "make_x_torch",
-           "make_expert_out_torch", "bf16_bits_from_f32"]
+           "make_expert_out", "make_expert_out_torch", "bf16_bits_from_f32"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -127,6 +127,17 @@ def make_x(w: Workload, seed: int | None = None, rows: int | None = None) -> np.
     rng = np.random.default_rng((w.seed if seed is None else seed) + 7919)
     T = w.num_tokens if rows is None else rows
     return bf16_bits_from_f32(rng.standard_normal((T, w.hidden), dtype=np.float32))
+
+
+def make_expert_out(rows: int, hidden: int, seed: int, chunk_rows: int = 16384) -> np.ndarray:
+    """A random expert output as bf16 bits (uint16) [rows, hidden] ~ N(0, 1),
+    generated on the host chunk by chunk (for the CPU-only timings)."""
+    rng = np.random.default_rng(seed + 15485863)
+    out = np.empty((rows, hidden), dtype=np.uint16)
+    for r0 in range(0, rows, chunk_rows):
+        r1 = min(rows, r0 + chunk_rows)
+        out[r0:r1] = bf16_bits_from_f32(rng.standard_normal((r1 - r0, hidden), dtype=np.float32))
+    return out
 
 
 def _randn_bf16_torch(rows: int, hidden: int, device, seed: int, chunk_rows: int = 65536):
