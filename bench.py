@@ -481,12 +481,17 @@ class GpuCase:
         if self.layer.device_status() != 0:
             raise SystemExit(f"device status {self.layer.device_status()} after warm-up ({self.w.name})")
 
-    def timed_steps(self, n):
+    def timed_steps(self, n, gate_s: float = 0.0):
         """Seconds of layout, dispatch and combine in each of n steps (CUDA
         events on the launching stream)."""
         import torch
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
         torch.cuda.synchronize(self.dev)
+        if gate_s > 0:
+            # hold the stream while the host enqueues the steps, so that no
+            # launch waits on the host (small layers take less GPU time per
+            # step than the Python calls that enqueue it); outside the events
+            torch.cuda._sleep(int(gate_s * 2.1e9))
         for i in range(n):
             self.flush.zero_()
             e = evs[i]

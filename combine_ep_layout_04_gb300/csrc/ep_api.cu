@@ -193,7 +193,7 @@ ep_status ep_create(const ep_config *cfg, ep_handle *out) {
         delete h;
         return EP_ERR_CUDA;
     }
-    h->tiles = static_cast<int>((T + 255) / 256);
+    h->tiles = static_cast<int>((T + ep::layout_tile(T) - 1) / ep::layout_tile(T));
     // log capacity: every message of every (s, d) with d in the busiest channel
     const int64_t ranks_per_chan = (R + C - 1) / C;
     const int64_t kmin = cfg->topk < ranks_per_chan ? cfg->topk : ranks_per_chan;

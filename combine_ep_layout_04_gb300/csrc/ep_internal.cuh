@@ -66,6 +66,9 @@ struct LayoutParams {
     int R, Tpr, E, K, Er, G;
     int tiles;
     int in_rank_vec;   // bytes per is_token_in_rank store: 16, 4 or 1
+    int slot_vec;      // 1: token_slot rows take 16-byte stores
+    int topk_vec4;     // 1: topk_idx rows take 16-byte loads
+    int er_shift;      // log2(E / R) when it is a power of two, else -1
 };
 
 // Dispatch kernel parameters.
@@ -155,6 +158,9 @@ ep_status launch_wait_signal(const unsigned long long *signal, unsigned long lon
 ep_status launch_expert_layout(ep_ctx *h, const int32_t *topk_idx, const float *topk_weights,
                                const ep_layout_out *lay, const ep_expert_layout_out *out,
                                int64_t recv_rows, int64_t rows_cap, cudaStream_t st);
+// Tokens per layout tile (one per thread) for T tokens (ep_layout.cu).
+int layout_tile(int64_t T);
+void fill_layout_vec(LayoutParams &p);
 // Rows per message G when ep_config.rows_per_msg is 0 (ep_api.cu).
 int default_rows_per_msg(int hidden);
 // Dispatch geometry, decided once per handle.

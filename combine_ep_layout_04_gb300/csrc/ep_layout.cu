@@ -8,116 +8,187 @@
 //   #{t' < t : in_rank[t'][d]}, and the small scans recv_off, send_off,
 //   msg_count, recv_count, recv_base, expert_off (definitions in include/ep.h).
 //
-// How: one CTA per tile of 256 tokens (one token per thread), tiles handed out
-// in launch order by a ticket counter so every tile's predecessors are
+// How: one CTA per tile of 256, 512 or 1024 tokens (one token per thread; the
+// tile grows with T so that large layers take about 128 tiles), tiles handed
+// out in launch order by a ticket counter so every tile's predecessors are
 // already running.  Per tile:
-//   1. read the K picks of each token; per-token rank mask; a histogram of
-//      picks per (source rank, expert) in shared memory (or, when the tile
-//      spans too many ranks, warp-aggregated global atomics via match_any);
-//   2. per destination column d: a warp ballot gives each token's position
-//      among the warp's members of d; warp totals give the tile aggregate;
-//   3. decoupled look-back (Merrill & Garland, "Single-pass Parallel Prefix
-//      Scan with Decoupled Look-back", 2016), one thread per column: publish
-//      the aggregate, walk back over predecessors' aggregates until an
-//      inclusive prefix is found, publish the inclusive prefix.  A descriptor
-//      is one 64-bit word {epoch:30 | flag:2 | value:32}; the epoch is derived
-//      from the ticket, so stale words from earlier calls are never taken and
-//      nothing has to be reset between calls (CUDA-graph safe);
-//   4. write, at each source rank's first token, the column prefix (from
+//   1. read the K picks of each token (16-byte loads when K % 4 == 0); per-token
+//      rank mask; a histogram of picks per (source rank, expert) in shared
+//      memory (or, when the tile spans too many ranks, warp-aggregated global
+//      atomics via match_any); the token's is_token_in_rank row;
+//   2. per destination column d: one warp ballot per column gives each
+//      token's position among its warp's members of d; a shuffle scan over
+//      the warps' counts gives each warp's offset and the tile's aggregate;
+//   3. the tile publishes its aggregates (one 64-bit word per column,
+//      {epoch:30 | flag:2 | value:32}; the epoch comes from the ticket, so
+//      stale words of earlier calls are never taken and nothing is reset
+//      between calls) and reads the aggregates of all its predecessors at
+//      once, every thread taking some (predecessor, column) pairs: one round
+//      trip instead of a walk.  With more than kAllPredMax tiles it falls back
+//      to decoupled look-back (Merrill & Garland, "Single-pass Parallel
+//      Prefix Scan with Decoupled Look-back", 2016), one thread per column;
+//   4. writes, at each source rank's first token, the column prefix (from
 //      which the last tile derives the per-(s, d) counts and all the small
-//      scans) and add the tile's histogram; fence; count the tile done;
-//   5. write token_slot (lane = column, coalesced) -- after the fence, which
-//      therefore does not wait for these stores; the last tile to finish
-//      then runs the small scans.
+//      scans) and adds its histogram; fence; counts the tile done;
+//   5. writes token_slot, each thread its token's row in 16-byte stores --
+//      after the fence, which therefore does not wait for these stores; the
+//      last tile to finish then runs the small scans, with every load of a
+//      batch issued before the first is used.
+#include <atomic>
+
 #include "ep_internal.cuh"
 
 namespace ep {
 namespace {
 
-constexpr int kTile = 256;
-constexpr int kWarps = kTile / 32;
+constexpr int kMaxTile = 1024;
+constexpr int kMaxWarps = kMaxTile / 32;
 constexpr int kHistCap = 4096;             // shared-memory histogram bins
+constexpr int kAllPredMax = 512;           // tiles up to which each tile sums all predecessors
+constexpr int kFinHistCap = 16384;         // R x E histograms the last tile stages in shared memory
 constexpr unsigned kFull = 0xffffffffu;
 
-// Exclusive scan of s[0, n) in place by the whole block (blockDim == kTile):
-// each thread scans a run of consecutive items, warps scan the run totals with
-// shuffles, one warp scans the warp totals.  Returns the total.  `tmp` holds
-// at least kWarps + 1 ints.
-__device__ int block_excl_scan(int *s, int n, int *tmp) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int per = (n + kTile - 1) / kTile;
-    const int b = tid * per, e = min(n, b + per);
-    int local = 0;
-    for (int i = b; i < e; ++i) local += s[i];
-    int incl = local;
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Exclusive scans of a[0, na) and b[0, nb) in place by the whole block, in
+// the same passes: each thread scans a run of consecutive items of each, warps
+// scan the run totals with shuffles, warps 0 and 1 scan the warp totals.
+// `tmp` holds at least 2 * kMaxWarps ints.
+__device__ void block_excl_scan2(int *a, int na, int *b, int nb, int *tmp) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, bd = blockDim.x, nw = bd >> 5;
+    const int pa = (na + bd - 1) / bd, pb = (nb + bd - 1) / bd;
+    const int a0 = min(na, tid * pa), a1 = min(na, a0 + pa), b0 = min(nb, tid * pb), b1 = min(nb, b0 + pb);
+    int la = 0, lb = 0;
+    for (int i = a0; i < a1; ++i) la += a[i];
+    for (int i = b0; i < b1; ++i) lb += b[i];
+    int ia = la, ib = lb;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += y;
+        const int ya = __shfl_up_sync(kFull, ia, o), yb = __shfl_up_sync(kFull, ib, o);
+        if (lane >= o) {
+            ia += ya;
+            ib += yb;
+        }
     }
-    if (lane == 31) tmp[warp] = incl;
+    if (lane == 31) {
+        tmp[warp] = ia;
+        tmp[kMaxWarps + warp] = ib;
+    }
     __syncthreads();
-    if (warp == 0) {
-        const int v = lane < kWarps ? tmp[lane] : 0;
+    if (warp < 2) {
+        int *tw = tmp + warp * kMaxWarps;
+        const int v = lane < nw ? tw[lane] : 0;
         int wi = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(kFull, wi, o);
             if (lane >= o) wi += y;
         }
-        if (lane < kWarps) tmp[lane] = wi - v;
-        if (lane == kWarps - 1) tmp[kWarps] = wi;
+        if (lane < nw) tw[lane] = wi - v;
     }
     __syncthreads();
-    int run = tmp[warp] + incl - local;
-    for (int i = b; i < e; ++i) {
-        const int v = s[i];
-        s[i] = run;
-        run += v;
+    int ra = tmp[warp] + ia - la, rb = tmp[kMaxWarps + warp] + ib - lb;
+    for (int i = a0; i < a1; ++i) {
+        const int v = a[i];
+        a[i] = ra;
+        ra += v;
     }
-    const int total = tmp[kWarps];
+    for (int i = b0; i < b1; ++i) {
+        const int v = b[i];
+        b[i] = rb;
+        rb += v;
+    }
     __syncthreads();
-    return total;
 }
 
-// The last tile to finish: counts and small scans from the column prefixes
-// and the histogram scratch; leaves the scratch zeroed for the next call.
-__device__ void finish_layout(const LayoutParams &p, int *s_work, int *s_tmp) {
-    const int tid = threadIdx.x;
-    const int R = p.R, E = p.E, G = p.G;
-    const int32_t *P = p.dev.col_prefix;
-    // per-(s, d) counts, window offsets, message counts: every load issued
-    // before the first store (P[i] and P[i + R] are the prefixes of (s, d)
-    // at the first tokens of ranks s and s + 1)
-    constexpr int kPairsPerThread = kMaxRanks * kMaxRanks / kTile;
-    int pa[kPairsPerThread], pb[kPairsPerThread];
-#pragma unroll
-    for (int q = 0; q < kPairsPerThread; ++q) {
-        const int i = tid + q * kTile;
-        if (i < R * R) {
-            pa[q] = __ldcg(P + i);
-            pb[q] = __ldcg(P + i + R);
-        }
+__host__ __device__ __forceinline__ int pad4(int n) { return (n + 3) & ~3; }
+
+// The finisher's staging area in dynamic shared memory (ints): the column
+// prefixes, the histogram (when R x E is at most kFinHistCap), the counts,
+// the expert totals.  The first two are 16-byte aligned for the bulk loads.
+struct FinLayout {
+    int oP, oH, oC, oT, total;
+    bool stage;
+    __host__ __device__ FinLayout(int R, int E) {
+        stage = R * E <= kFinHistCap;
+        oP = 0;
+        oH = pad4((R + 1) * R);
+        oC = oH + (stage ? pad4(R * E) : 0);
+        oT = oC + R * R;
+        total = oT + E;
     }
-#pragma unroll
-    for (int q = 0; q < kPairsPerThread; ++q) {
-        const int i = tid + q * kTile;
-        if (i >= R * R) break;
-        const int c = pb[q] - pa[q];
-        p.out.num_tokens_per_rank[i] = c;
-        p.out.recv_off[i] = pa[q];
-        p.out.msg_count[i] = (c + G - 1) / G;
-        s_work[i] = c;
+};
+
+// The finisher: the CTA that drew the call's last ticket.  It waits until
+// every tile has counted itself done, brings the column prefixes and the
+// histogram into shared memory with two bulk copies, derives the counts and
+// the small scans there, and stores everything at the end; it leaves the
+// histogram scratch and the done counter zeroed for the next call.
+__device__ void finish_layout(const LayoutParams &p, int *fin, int *s_tmp, uint64_t *bar) {
+    const int tid = threadIdx.x, bd = blockDim.x;
+    const int R = p.R, E = p.E, G = p.G, RR = R * R;
+    const FinLayout f(R, E);
+    int *fP = fin + f.oP, *fH = fin + f.oH, *fC = fin + f.oC, *fT = fin + f.oT;
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_fence_init();
+        const uint64_t t_start = globaltimer_ns();
+        uint32_t spins = 0;
+        while (ld_acquire_u32(p.dev.done) < static_cast<unsigned>(p.tiles)) {
+            if ((++spins & 15u) == 0u && globaltimer_ns() - t_start > kDefaultTimeoutNs) {
+                set_error(p.dev.err, EP_ERR_TIMEOUT);
+                break;
+            }
+            __nanosleep(32);
+        }
+        // the tiles' writes (generic proxy) are acquired; the bulk copies
+        // below read them through the async proxy
+        fence_proxy_async_global();
+        // sizes rounded up to 16 bytes: both regions are followed by padding
+        // in the scratch carve
+        const uint32_t bP = static_cast<uint32_t>(pad4((R + 1) * R) * 4);
+        const uint32_t bH = f.stage ? static_cast<uint32_t>(pad4(R * E) * 4) : 0u;
+        mbar_arrive_expect_tx(bar, bP + bH);
+        bulk_g2s(fP, p.dev.col_prefix, bP, bar);
+        if (f.stage) bulk_g2s(fH, p.dev.hist, bH, bar);
     }
     __syncthreads();
-    block_excl_scan(s_work, R * R, s_tmp);   // row-major send order
-    for (int i = tid; i < R * R; i += kTile) p.out.send_off[i] = s_work[i];
-    // window sizes and starts (one warp)
+    if (!mbar_wait_bounded(bar, 0u, nullptr, kDefaultTimeoutNs)) set_error(p.dev.err, EP_ERR_TIMEOUT);
+    for (int i = tid; i < RR; i += bd) fC[i] = fP[i + R] - fP[i];
+    if (f.stage) {
+        for (int e = tid; e < E; e += bd) {
+            int tot = 0;
+            for (int s = 0; s < R; ++s) tot += fH[s * E + e];
+            fT[e] = tot;
+        }
+    } else {
+        // large R x E: each thread sums one expert from global memory
+        for (int e = tid; e < E; e += bd) {
+            int tot = 0;
+            for (int s0 = 0; s0 < R; s0 += 8) {
+                int v[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    v[q] = s0 + q < R ? __ldcg(p.dev.hist + static_cast<int64_t>(s0 + q) * E + e) : 0;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) tot += v[q];
+            }
+            fT[e] = tot;
+        }
+    }
+    __syncthreads();
+    block_excl_scan2(fC, RR, fT, E, s_tmp);   // row-major send order; expert offsets
+    // window sizes and starts (one warp), then every store
     if (tid < 32) {
         int64_t run = 0;
-        for (int d0 = 0; d0 < R; d0 += 32) {
-            const int d = d0 + tid;
-            const int c = d < R ? __ldcg(P + R * R + d) : 0;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            const int d = g * 32 + tid;
+            const int c = d < R ? fP[RR + d] : 0;
             int incl = c;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -130,74 +201,132 @@ __device__ void finish_layout(const LayoutParams &p, int *s_work, int *s_tmp) {
             }
             run += __shfl_sync(kFull, incl, 31);
         }
-        if (tid == 0) *p.dev.n_recv = run;
-    }
-    __syncthreads();
-    // expert totals: each thread sums one expert over the source ranks,
-    // copying the histogram out and clearing the scratch as it goes
-    for (int e = tid; e < E; e += kTile) {
-        int tot = 0;
-        for (int s0 = 0; s0 < R; s0 += 8) {   // eight loads in flight, then their stores
-            int v[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                v[q] = s0 + q < R ? __ldcg(p.dev.hist + static_cast<int64_t>(s0 + q) * E + e) : 0;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                if (s0 + q >= R) break;
-                p.out.num_tokens_per_expert[static_cast<int64_t>(s0 + q) * E + e] = v[q];
-                p.dev.hist[static_cast<int64_t>(s0 + q) * E + e] = 0;
-                tot += v[q];
-            }
+        if (tid == 0) {
+            *p.dev.n_recv = run;
+            *p.dev.done = 0u;
         }
-        s_work[e] = tot;
     }
-    __syncthreads();
-    block_excl_scan(s_work, E, s_tmp);
-    for (int e = tid; e < E; e += kTile) p.out.expert_off[e] = s_work[e];
-    if (tid == 0) *p.dev.done = 0u;
+    for (int i = tid; i < RR; i += bd) {
+        const int c = fP[i + R] - fP[i];
+        p.out.num_tokens_per_rank[i] = c;
+        p.out.recv_off[i] = fP[i];
+        p.out.msg_count[i] = (c + G - 1) / G;
+        p.out.send_off[i] = fC[i];
+    }
+    for (int e = tid; e < E; e += bd) p.out.expert_off[e] = fT[e];
+    for (int i = tid; i < R * E; i += bd) {
+        p.out.num_tokens_per_expert[i] = f.stage ? fH[i] : __ldcg(p.dev.hist + i);
+        p.dev.hist[i] = 0;
+    }
 }
 
-__global__ void __launch_bounds__(kTile) layout_kernel(const LayoutParams p) {
-    __shared__ int s_wcnt[kWarps][kMaxRanks];
-    __shared__ int s_excl[kMaxRanks];
-    __shared__ int s_agg[kMaxRanks];
+__global__ void __launch_bounds__(kMaxTile) layout_kernel(const LayoutParams p) {
+    __shared__ __align__(16) unsigned s_ballot[kMaxWarps][kMaxRanks];   // per warp and column: members among its 32 tokens
+    __shared__ __align__(16) int s_woff[kMaxWarps][kMaxRanks];          // per warp and column: members in earlier warps
+    __shared__ __align__(16) int s_excl[kMaxRanks];                     // per column: members in earlier tiles
+    __shared__ int s_agg[kMaxRanks];                                    // per column: members in this tile
     __shared__ int s_hist[kHistCap];
-    __shared__ int s_tmp[kTile + 1];
+    __shared__ int s_tmp[2 * kMaxWarps];
+    __shared__ unsigned long long s_mask[kMaxTile];                     // rank mask of each token of the tile
     __shared__ unsigned long long s_ticket;
-    __shared__ int s_is_last;
+    __shared__ __align__(8) uint64_t s_bar;
+    extern __shared__ __align__(16) int fin[];                          // the finisher's staging
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int R = p.R, E = p.E, K = p.K, Er = p.Er, Tpr = p.Tpr;
+    const int bd = blockDim.x, nw = bd >> 5;
+    const int R = p.R, E = p.E, K = p.K, Tpr = p.Tpr;
 
     if (tid == 0) s_ticket = atomicAdd(p.dev.ticket, 1ull);
+    if (tid < R) s_excl[tid] = 0;
     __syncthreads();
-    const unsigned long long ticket = s_ticket;
-    const int tile = static_cast<int>(ticket % static_cast<unsigned long long>(p.tiles));
-    const uint32_t epoch = static_cast<uint32_t>((ticket / p.tiles) % ((1u << 30) - 1u)) + 1u;
+    // tickets of one call: tiles 0 .. tiles-1 in order, then the finisher
+    const unsigned long long ticket = s_ticket, per_call = static_cast<unsigned long long>(p.tiles) + 1ull;
+    const int tile = static_cast<int>(ticket % per_call);
+    const uint32_t epoch = static_cast<uint32_t>((ticket / per_call) % ((1u << 30) - 1u)) + 1u;
+    if (tile == p.tiles) {
+        finish_layout(p, fin, s_tmp, &s_bar);
+        return;
+    }
 
-    const int64_t t0 = static_cast<int64_t>(tile) * kTile;
-    const int nt = static_cast<int>(min(static_cast<int64_t>(kTile), p.T - t0));
-    const int s_first = static_cast<int>(t0 / Tpr);
-    const int s_last = static_cast<int>((t0 + nt - 1) / Tpr);
+    // T < 2^31 (ep_config_check), so token numbers fit in 32 bits
+    const int t0 = tile * bd;
+    const int nt = min(bd, static_cast<int>(p.T) - t0);
+    const int t = t0 + tid;
+    const bool valid = tid < nt;
+    const int s_first = t0 / Tpr;
+    const int s_last = (t0 + nt - 1) / Tpr;
     const int span = s_last - s_first + 1;
     const bool smem_hist = span * E <= kHistCap;
+    const int s_tok = valid ? t / Tpr : s_first;
+
+    // 1. picks -> rank mask (the histogram waits until the aggregates are out)
+    const int32_t *prow = p.topk_idx + static_cast<int64_t>(t) * K;
+    unsigned long long mask = 0ull;
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        int ev[8];
+        if (p.topk_vec4 && k0 + 8 <= K) {
+            const int4 a = valid ? __ldg(reinterpret_cast<const int4 *>(prow + k0)) : make_int4(-1, -1, -1, -1);
+            const int4 b = valid ? __ldg(reinterpret_cast<const int4 *>(prow + k0 + 4)) : make_int4(-1, -1, -1, -1);
+            ev[0] = a.x; ev[1] = a.y; ev[2] = a.z; ev[3] = a.w;
+            ev[4] = b.x; ev[5] = b.y; ev[6] = b.z; ev[7] = b.w;
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) ev[q] = (valid && k0 + q < K) ? __ldg(prow + k0 + q) : -1;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int e = ev[q];
+            if (e < -1 || e >= E) set_error(p.dev.err, EP_ERR_INVALID_ARG);
+            else if (e >= 0) mask |= 1ull << (p.er_shift >= 0 ? (e >> p.er_shift) : (e / p.Er));
+        }
+    }
+    s_mask[tid] = mask;
     if (smem_hist)
-        for (int i = tid; i < span * E; i += kTile) s_hist[i] = 0;
+        for (int i = tid; i < span * E; i += bd) s_hist[i] = 0;
+
+    // 2. per 32-column group, transpose the warp's 32 x 32 bit matrix (row =
+    //    token, column = rank) in five shuffle rounds, so that lane j holds
+    //    column j's bits over the warp's tokens
+    const int ngroups = (R + 31) >> 5;
+#pragma unroll
+    for (int g = 0; g < kMaxRanks / 32; ++g) {
+        if (g >= ngroups) break;
+        unsigned x = static_cast<unsigned>(mask >> (32 * g));
+#pragma unroll
+        for (int sft = 16; sft > 0; sft >>= 1) {
+            const unsigned m = sft == 16 ? 0x0000FFFFu : sft == 8 ? 0x00FF00FFu : sft == 4 ? 0x0F0F0F0Fu
+                             : sft == 2 ? 0x33333333u : 0x55555555u;
+            const unsigned y = __shfl_xor_sync(kFull, x, sft);
+            x = (lane & sft) ? ((x & ~m) | ((y & ~m) >> sft)) : ((x & m) | ((y & m) << sft));
+        }
+        if (g * 32 + lane < R) s_ballot[warp][g * 32 + lane] = x;
+    }
+    __syncthreads();
+    // per column: warps' member counts scanned across the warps
+    for (int d = warp; d < R; d += nw) {
+        const int c = lane < nw ? __popc(s_ballot[lane][d]) : 0;
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane < nw) s_woff[lane][d] = incl - c;
+        if (lane == 31) s_agg[d] = incl;
+    }
     __syncthreads();
 
-    // 1. picks -> rank mask and histogram
-    const int64_t t = t0 + tid;
-    const bool valid = tid < nt;
-    const int s_tok = valid ? static_cast<int>(t / Tpr) : 0;
-    unsigned long long mask = 0ull;
+    // 3. publish this tile's aggregates; the histogram of the picks (read again,
+    //    from cache); then the predecessors' aggregates
+    unsigned long long *desc = p.dev.tile_desc;
+    const bool all_pred = p.tiles <= kAllPredMax;
+    if (tid < R)
+        st_relaxed(desc + static_cast<int64_t>(tile) * R + tid,
+                   look_desc(epoch, (tile == 0 && !all_pred) ? kLookPrefix : kLookAggregate,
+                             static_cast<uint32_t>(s_agg[tid])));
     for (int k = 0; k < K; ++k) {
-        int e = valid ? __ldg(p.topk_idx + t * K + k) : -1;
-        if (e < -1 || e >= E) {
-            set_error(p.dev.err, EP_ERR_INVALID_ARG);
-            e = -1;
-        }
-        if (e >= 0) mask |= 1ull << (e / Er);
+        int e = valid ? __ldg(prow + k) : -1;
+        if (e < -1 || e >= E) e = -1;
         if (smem_hist) {
             if (e >= 0) atomicAdd(&s_hist[(s_tok - s_first) * E + e], 1);
         } else {
@@ -206,127 +335,146 @@ __global__ void __launch_bounds__(kTile) layout_kernel(const LayoutParams p) {
             if (key >= 0 && lane == __ffs(peers) - 1) atomicAdd(p.dev.hist + key, __popc(peers));
         }
     }
-
-    // is_token_in_rank row of this token
-    if (valid) {
-        uint8_t *row = p.out.is_token_in_rank + t * R;
-        if (p.in_rank_vec == 16) {
-            for (int d = 0; d < R; d += 16) {
-                uint32_t w[4];
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t v = 0;
-                    for (int b = 0; b < 4; ++b) v |= static_cast<uint32_t>((mask >> (d + 4 * q + b)) & 1ull) << (8 * b);
-                    w[q] = v;
+    if (tile > 0) {
+        const uint64_t t_start = globaltimer_ns();
+        if (all_pred) {
+            // thread tid takes column tid % R of predecessors tid / R, + step, ...
+            const int step = bd / R;
+            const int d = tid % R, j0 = tid / R;
+            if (j0 < step) {
+                int sum = 0;
+                for (int jb = j0; jb < tile; jb += 8 * step) {
+                    unsigned long long v[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int j = jb + q * step;
+                        v[q] = j < tile ? ld_relaxed(desc + static_cast<int64_t>(j) * R + d) : 0ull;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int j = jb + q * step;
+                        if (j >= tile) break;
+                        unsigned long long x = v[q];
+                        uint32_t spins = 0;
+                        while (static_cast<uint32_t>(x >> 34) != epoch || ((x >> 32) & 3u) != kLookAggregate) {
+                            if ((++spins & 15u) == 0u && globaltimer_ns() - t_start > kDefaultTimeoutNs) {
+                                set_error(p.dev.err, EP_ERR_TIMEOUT);
+                                x = 0ull;
+                                break;
+                            }
+                            __nanosleep(32);
+                            x = ld_relaxed(desc + static_cast<int64_t>(j) * R + d);
+                        }
+                        sum += static_cast<int>(static_cast<uint32_t>(x));
+                    }
                 }
-                *reinterpret_cast<uint4 *>(row + d) = make_uint4(w[0], w[1], w[2], w[3]);
+                if (sum) atomicAdd(&s_excl[d], sum);
             }
-        } else if (p.in_rank_vec == 4) {
-            for (int d = 0; d < R; d += 4) {
-                uint32_t v = 0;
-                for (int b = 0; b < 4; ++b) v |= static_cast<uint32_t>((mask >> (d + b)) & 1ull) << (8 * b);
-                *reinterpret_cast<uint32_t *>(row + d) = v;
-            }
-        } else {
-            for (int d = 0; d < R; ++d) row[d] = static_cast<uint8_t>((mask >> d) & 1ull);
-        }
-    }
-
-    // 2. per-column ballots: lane j of each 32-column group keeps column j's bits
-    const int ngroups = (R + 31) / 32;
-    unsigned colbits[kMaxRanks / 32];
-#pragma unroll
-    for (int g = 0; g < kMaxRanks / 32; ++g) {
-        colbits[g] = 0u;
-        if (g < ngroups) {
-            const int ncol = min(32, R - g * 32);
-            for (int j = 0; j < ncol; ++j) {
-                const unsigned b = __ballot_sync(kFull, (mask >> (g * 32 + j)) & 1ull);
-                if (lane == j) colbits[g] = b;
-            }
-            const int d = g * 32 + lane;
-            if (d < R) s_wcnt[warp][d] = __popc(colbits[g]);
+        } else if (tid < R) {
+            const int excl = lookback_excl(desc, R, tid, tile, epoch, t_start, kDefaultTimeoutNs, p.dev.err);
+            s_excl[tid] = excl;
+            st_relaxed(desc + static_cast<int64_t>(tile) * R + tid,
+                       look_desc(epoch, kLookPrefix, static_cast<uint32_t>(excl + s_agg[tid])));
         }
     }
     __syncthreads();
-    if (tid < R) {
-        int run = 0;
-        for (int w = 0; w < kWarps; ++w) {
-            const int v = s_wcnt[w][tid];
-            s_wcnt[w][tid] = run;
-            run += v;
-        }
-        s_agg[tid] = run;
-    }
-    __syncthreads();
 
-    // 3. decoupled look-back, one thread per column
-    if (tid < R) {
-        const int d = tid;
-        const int agg = s_agg[d];
-        unsigned long long *mine = p.dev.tile_desc + static_cast<int64_t>(tile) * R + d;
-        int excl = 0;
-        if (tile == 0) {
-            st_relaxed(mine, look_desc(epoch, kLookPrefix, static_cast<uint32_t>(agg)));
-        } else {
-            st_relaxed(mine, look_desc(epoch, kLookAggregate, static_cast<uint32_t>(agg)));
-            excl = lookback_excl(p.dev.tile_desc, R, d, tile, epoch, globaltimer_ns(), kDefaultTimeoutNs, p.dev.err);
-            st_relaxed(mine, look_desc(epoch, kLookPrefix, static_cast<uint32_t>(excl + agg)));
-        }
-        s_excl[d] = excl;
-        if (tile == p.tiles - 1) p.dev.col_prefix[R * R + d] = excl + agg;
-    }
-    __syncthreads();
-
-    // 4. the column prefix at the first token of each source rank that
-    //    starts in this tile, and the tile's histogram: the last tile reads
-    //    both, so they go out before the fence
-#pragma unroll
-    for (int g = 0; g < kMaxRanks / 32; ++g) {
-        const int d = g * 32 + lane;
-        if (g >= ngroups || d >= R) continue;
-        const unsigned bits = colbits[g];
-        const int base = s_excl[d] + s_wcnt[warp][d];
-        for (int64_t s = (t0 + Tpr - 1) / Tpr; s * Tpr < t0 + nt; ++s) {
-            const int j = static_cast<int>(s * Tpr - t0) - warp * 32;
-            if (j < 0 || j >= 32) continue;
-            p.dev.col_prefix[s * R + d] = base + __popc(bits & ((1u << j) - 1u));
-        }
+    // 4. what the finisher reads -- the column prefix at the first token of
+    //    each source rank that starts here, the column totals (last tile by
+    //    position) and the histogram -- goes out before the fence
+    const unsigned lt = lanemask_lt();
+    if (tile == p.tiles - 1 && tid < R) p.dev.col_prefix[R * R + tid] = s_excl[tid] + s_agg[tid];
+    if (valid && t == s_tok * Tpr) {
+        int32_t *pr = p.dev.col_prefix + static_cast<int64_t>(s_tok) * R;
+        for (int d = 0; d < R; ++d) pr[d] = s_excl[d] + s_woff[warp][d] + __popc(s_ballot[warp][d] & lt);
     }
     if (smem_hist) {
-        __syncthreads();
-        for (int i = tid; i < span * E; i += kTile) {
+        for (int i = tid; i < span * E; i += bd) {
             const int v = s_hist[i];
             if (v) atomicAdd(p.dev.hist + static_cast<int64_t>(s_first) * E + i, v);
         }
     }
-
-    // 5. count this tile done; the last one to finish derives the small scans
     __threadfence();
     __syncthreads();
-    if (tid == 0) s_is_last = (atomicAdd(p.dev.done, 1u) == static_cast<unsigned>(p.tiles - 1));
+    if (tid == 0) atomicAdd(p.dev.done, 1u);
 
-    // 6. token_slot, lane = column (nothing in this kernel reads it back, so
-    //    the fence above does not wait for these stores)
+    // 5. the tile's rows of is_token_in_rank and token_slot, last: no barrier
+    //    follows them.  A warp's 32 rows are contiguous; each lane stores
+    //    16-byte pieces of them, so every store instruction covers whole lines.
+    const int wt0 = t0 + warp * 32;                       // the warp's first token
+    const int wn = max(0, min(32, nt - warp * 32));       // its tokens
+    if (p.in_rank_vec == 16) {
+        uint8_t *base = p.out.is_token_in_rank + static_cast<int64_t>(wt0) * R;
+        for (int c = lane; c < wn * R / 16; c += 32) {    // piece c: token c*16/R, columns (c*16) % R ..
+            const int j = c * 16 / R, d0 = (c * 16) % R;
+            const unsigned long long m = s_mask[warp * 32 + j];
+            uint32_t w[4];
 #pragma unroll
-    for (int g = 0; g < kMaxRanks / 32; ++g) {
-        const int d = g * 32 + lane;
-        if (g >= ngroups || d >= R) continue;
-        const unsigned bits = colbits[g];
-        const int base = s_excl[d] + s_wcnt[warp][d];
-        for (int j = 0; j < 32; ++j) {
-            const int local = warp * 32 + j;
-            if (local >= nt) break;
-            const int64_t tt = t0 + local;
-            p.out.token_slot[tt * R + d] = ((bits >> j) & 1u) ? base + __popc(bits & ((1u << j) - 1u)) : -1;
+            for (int q = 0; q < 4; ++q) {
+                // four mask bits -> four bytes of 0/1
+                const uint32_t nib = static_cast<uint32_t>(m >> (d0 + 4 * q)) & 0xFu;
+                w[q] = (nib * 0x00204081u) & 0x01010101u;
+            }
+            *reinterpret_cast<uint4 *>(base + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
         }
+    } else if (valid) {
+        uint8_t *row = p.out.is_token_in_rank + static_cast<int64_t>(t) * R;
+        for (int d = 0; d < R; ++d) row[d] = static_cast<uint8_t>((mask >> d) & 1ull);
     }
-    __syncthreads();
-    if (!s_is_last) return;
-    __threadfence();
-    finish_layout(p, s_hist, s_tmp);
+    if (p.slot_vec) {
+        int32_t *base = p.out.token_slot + static_cast<int64_t>(wt0) * R;
+        for (int c = lane; c < wn * R / 4; c += 32) {     // piece c: token c*4/R, columns (c*4) % R ..
+            const int j = c * 4 / R, d0 = (c * 4) % R;
+            const unsigned below = (1u << j) - 1u;
+            const uint4 b = *reinterpret_cast<const uint4 *>(&s_ballot[warp][d0]);
+            const int4 wo = *reinterpret_cast<const int4 *>(&s_woff[warp][d0]);
+            const int4 ex = *reinterpret_cast<const int4 *>(&s_excl[d0]);
+            int4 v;
+            v.x = ((b.x >> j) & 1u) ? ex.x + wo.x + __popc(b.x & below) : -1;
+            v.y = ((b.y >> j) & 1u) ? ex.y + wo.y + __popc(b.y & below) : -1;
+            v.z = ((b.z >> j) & 1u) ? ex.z + wo.z + __popc(b.z & below) : -1;
+            v.w = ((b.w >> j) & 1u) ? ex.w + wo.w + __popc(b.w & below) : -1;
+            *reinterpret_cast<int4 *>(base + c * 4) = v;
+        }
+    } else if (valid) {
+        int32_t *srow = p.out.token_slot + static_cast<int64_t>(t) * R;
+        for (int d = 0; d < R; ++d)
+            srow[d] = ((mask >> d) & 1ull) ? s_excl[d] + s_woff[warp][d] + __popc(s_ballot[warp][d] & lt) : -1;
+    }
 }
 
 }  // namespace
+
+int layout_tile(int64_t T) { return T <= 16384 ? 256 : T <= 65536 ? 512 : kMaxTile; }
+
+// Dynamic shared memory of the layout kernel: the finisher's staging area.
+size_t layout_smem_bytes(int R, int E) { return static_cast<size_t>(FinLayout(R, E).total) * 4; }
+
+// Allows the kernel the largest staging area any shape asks for, once per
+// device (R = 64 with R x E at the staging cap is the largest).
+ep_status layout_prepare() {
+    constexpr int kDevs = 64;
+    static std::atomic<int> ready[kDevs];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return EP_ERR_CUDA;
+    if (ready[dev].load(std::memory_order_acquire)) return EP_OK;
+    size_t most = 0;
+    for (int R = 1; R <= kMaxRanks; ++R)
+        for (int E = R; E <= 4096; E += R) most = most > layout_smem_bytes(R, E) ? most : layout_smem_bytes(R, E);
+    if (cudaFuncSetAttribute(layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(most)) !=
+        cudaSuccess)
+        return EP_ERR_CUDA;
+    ready[dev].store(1, std::memory_order_release);
+    return EP_OK;
+}
+
+void fill_layout_vec(LayoutParams &p) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p.out.is_token_in_rank);
+    p.in_rank_vec = (p.R % 16 == 0 && a % 16 == 0) ? 16 : (p.R % 4 == 0 && a % 4 == 0) ? 4 : 1;
+    p.slot_vec = (p.R % 4 == 0 && reinterpret_cast<uintptr_t>(p.out.token_slot) % 16 == 0) ? 1 : 0;
+    p.topk_vec4 = (p.K % 4 == 0 && reinterpret_cast<uintptr_t>(p.topk_idx) % 16 == 0) ? 1 : 0;
+    p.er_shift = (p.Er & (p.Er - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(p.Er)) : -1;
+}
 
 ep_status launch_layout(ep_ctx *h, const int32_t *topk_idx, const ep_layout_out *out, cudaStream_t st) {
     LayoutParams p{};
@@ -341,9 +489,10 @@ ep_status launch_layout(ep_ctx *h, const int32_t *topk_idx, const ep_layout_out 
     p.Er = p.E / p.R;
     p.G = h->G;
     p.tiles = h->tiles;
-    const uintptr_t a = reinterpret_cast<uintptr_t>(out->is_token_in_rank);
-    p.in_rank_vec = (p.R % 16 == 0 && a % 16 == 0) ? 16 : (p.R % 4 == 0 && a % 4 == 0) ? 4 : 1;
-    layout_kernel<<<h->tiles, kTile, 0, st>>>(p);
+    fill_layout_vec(p);
+    if (layout_prepare() != EP_OK) return EP_ERR_CUDA;
+    // the token tiles, plus the finisher
+    layout_kernel<<<h->tiles + 1, layout_tile(p.T), layout_smem_bytes(p.R, p.E), st>>>(p);
     return cudaGetLastError() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }
 
@@ -434,7 +583,8 @@ extern "C" ep_status ep_layout_static(const ep_config *cfg, const int32_t *topk_
     p.K = cfg->topk;
     p.Er = p.E / p.R;
     p.G = cfg->rows_per_msg ? cfg->rows_per_msg : default_rows_per_msg(cfg->hidden);
-    p.tiles = static_cast<int>((T + 255) / 256);
+    const int tile_tokens = layout_tile(T);
+    p.tiles = static_cast<int>((T + tile_tokens - 1) / tile_tokens);
     p.dev.err = reinterpret_cast<int32_t *>(b + kSErr);
     p.dev.ticket = reinterpret_cast<unsigned long long *>(b + kSTicket);
     p.dev.done = reinterpret_cast<unsigned int *>(b + kSDone);
@@ -442,15 +592,15 @@ extern "C" ep_status ep_layout_static(const ep_config *cfg, const int32_t *topk_
     p.dev.col_prefix = reinterpret_cast<int32_t *>(b + kSPrefix);
     p.dev.hist = reinterpret_cast<int32_t *>(b + kSHist);
     p.dev.tile_desc = reinterpret_cast<unsigned long long *>(b + kSDesc);
-    const uintptr_t a = reinterpret_cast<uintptr_t>(out->is_token_in_rank);
-    p.in_rank_vec = (p.R % 16 == 0 && a % 16 == 0) ? 16 : (p.R % 4 == 0 && a % 4 == 0) ? 4 : 1;
+    fill_layout_vec(p);
     // The array keeps the last call's contents: clear what this call needs at
     // zero (counters, error word, histogram, look-back descriptors).
     if (cudaMemsetAsync(b, 0, kSPrefix, st) != cudaSuccess ||
         cudaMemsetAsync(b + kSHist, 0, static_cast<size_t>(p.R) * p.E * 4, st) != cudaSuccess ||
         cudaMemsetAsync(b + kSDesc, 0, static_cast<size_t>(p.tiles) * p.R * 8, st) != cudaSuccess)
         return EP_ERR_CUDA;
-    layout_kernel<<<p.tiles, kTile, 0, st>>>(p);
+    if (layout_prepare() != EP_OK) return EP_ERR_CUDA;
+    layout_kernel<<<p.tiles + 1, tile_tokens, layout_smem_bytes(p.R, p.E), st>>>(p);
     if (cudaGetLastError() != cudaSuccess) return EP_ERR_CUDA;
     if (!n_recv_host) return EP_OK;
     int64_t n = 0;
