@@ -202,6 +202,39 @@ struct Bars {
     uint64_t *stage_full, *meta_full, *meta_free, *stage_empty;
 };
 
+// The chunks a copy CTA copies, in order: its first is fixed (copy CTA i
+// takes chunk i of the call), the rest come from a device-wide counter, so
+// that CTAs on faster SMs take more and all finish together.  Each draw
+// publishes the chunk id to the CTA's other warps first and only then asks
+// the counter for the next one, so that the atomic's round trip overlaps a
+// whole chunk of copying instead of delaying the release.  Warp-uniform.
+struct ChunkDraw {
+    const DispatchParams &p;
+    unsigned long long *words;
+    int *ids;
+    unsigned int ahead;   // lane 0: index (within the call) of the next chunk
+    int n_drawn = 0;
+    __device__ ChunkDraw(const DispatchParams &p_, unsigned long long *w, int *i)
+        : p(p_), words(w), ids(i), ahead(blockIdx.x - static_cast<unsigned>(p_.C)) {}
+    __device__ int next() {
+        const int lane = threadIdx.x & 31;
+        const unsigned ncopy = gridDim.x - static_cast<unsigned>(p.C);
+        int k = -1;
+        if (lane == 0) {
+            k = ahead < static_cast<unsigned>(p.k1 - p.k0) ? p.k0 + static_cast<int>(ahead) : -1;
+            ids[n_drawn % kIdSlots] = k;
+        }
+        k = __shfl_sync(kFull, k, 0);
+        ++n_drawn;
+        __syncwarp();
+        if (lane == 0) {
+            st_release_cta_shared(&words[kWIds], static_cast<unsigned long long>(n_drawn));
+            if (k >= 0) ahead = ncopy + atomicAdd(p.dev.chunk_next, 1u);
+        }
+        return k;
+    }
+};
+
 // ------------------------------------------------------------ copy CTA: copy
 // Chunks are drawn from a device-wide counter as the loads reach them, so
 // that CTAs on faster SMs take more chunks and all finish together; the ids
@@ -218,24 +251,8 @@ __device__ void copy_warp(const DispatchParams &p, uint8_t *smem, const SmemLayo
     for (int i = 0; i < kDoneSlots; ++i) last_item[i] = 0;
     bool ok = true;
 
-    // the next chunk id is drawn one chunk ahead so that its atomic's round
-    // trip overlaps a whole chunk of copying
-    unsigned int ahead = 0;
-    if (lane == 0) ahead = atomicAdd(p.dev.chunk_next, 1u);
-    int n_drawn = 0;
-    auto draw = [&]() -> int {   // warp-uniform
-        int k = -1;
-        if (lane == 0) {
-            k = ahead < static_cast<unsigned>(p.k1 - p.k0) ? p.k0 + static_cast<int>(ahead) : -1;
-            if (k >= 0) ahead = atomicAdd(p.dev.chunk_next, 1u);
-            ids[n_drawn % kIdSlots] = k;
-        }
-        k = __shfl_sync(kFull, k, 0);
-        ++n_drawn;
-        __syncwarp();
-        if (lane == 0) st_release_cta_shared(&words[kWIds], static_cast<unsigned long long>(n_drawn));
-        return k;
-    };
+    ChunkDraw dr(p, words, ids);
+    auto draw = [&]() -> int { return dr.next(); };
     ItemCursor ld, stc;
     int ld_m = 0, st_m = 0;
     ld.set_chunk(p, draw());
@@ -369,22 +386,8 @@ __device__ void copy_warp_vec(const DispatchParams &p, uint8_t *smem, const Smem
     for (int i = 0; i < kDoneSlots; ++i) last_item[i] = 0;
     bool ok = true;
 
-    unsigned int ahead = 0;
-    if (lane == 0) ahead = atomicAdd(p.dev.chunk_next, 1u);
-    int n_drawn = 0;
-    auto draw = [&]() -> int {   // warp-uniform
-        int k = -1;
-        if (lane == 0) {
-            k = ahead < static_cast<unsigned>(p.k1 - p.k0) ? p.k0 + static_cast<int>(ahead) : -1;
-            if (k >= 0) ahead = atomicAdd(p.dev.chunk_next, 1u);
-            ids[n_drawn % kIdSlots] = k;
-        }
-        k = __shfl_sync(kFull, k, 0);
-        ++n_drawn;
-        __syncwarp();
-        if (lane == 0) st_release_cta_shared(&words[kWIds], static_cast<unsigned long long>(n_drawn));
-        return k;
-    };
+    ChunkDraw dr(p, words, ids);
+    auto draw = [&]() -> int { return dr.next(); };
     // take back the items the store warps have finished, in order; report the
     // chunks whose every item is back.  Blocking: wait until item `until` is.
     auto take_back = [&](int64_t until) {
@@ -470,6 +473,7 @@ __device__ void store_warp(const DispatchParams &p, uint8_t *smem, const SmemLay
         const uint32_t par = static_cast<uint32_t>(i / S) & 1u;
         // item i, once loaded, or the end
         const uint64_t t0 = globaltimer_ns();
+        ErrPoll ep(t0);
         bool have = false, end = false;
         unsigned nap = 32;
         while (true) {
@@ -480,7 +484,8 @@ __device__ void store_warp(const DispatchParams &p, uint8_t *smem, const SmemLay
                 end = true;
                 break;
             }
-            bool give_up = read_error(p.dev.err) != 0 || globaltimer_ns() - t0 > p.timeout_ns;
+            const uint64_t now = globaltimer_ns();
+            bool give_up = (lane == 0 && ep.raised(p.dev.err, now)) || now - t0 > p.timeout_ns;
             if (__any_sync(kFull, give_up)) {
                 if (read_error(p.dev.err) == 0) set_error(p.dev.err, EP_ERR_TIMEOUT);
                 end = true;
@@ -526,7 +531,7 @@ __device__ void store_warp(const DispatchParams &p, uint8_t *smem, const SmemLay
 }
 
 // ------------------------------------------------------------ copy CTA: meta
-__device__ void build_meta(const DispatchParams &p, int k, const MetaSlot &ms, const int *rbase) {
+__device__ void build_meta_by_token(const DispatchParams &p, int k, const MetaSlot &ms, const int *rbase) {
     const int lane = threadIdx.x & 31;
     const int R = p.R;
     const int ntok = chunk_ntok(p, k);
@@ -536,9 +541,11 @@ __device__ void build_meta(const DispatchParams &p, int k, const MetaSlot &ms, c
     int32_t *notice = p.dev.notice + static_cast<int64_t>(k) * 2 * R;
     int n = 0;
     int *dst = ms.dst + lane * R;
-    // token_slot row of this lane's token, kMetaLoads x 4 destinations per
+    // lane = token.  Its token_slot row, kMetaLoads x 4 destinations per
     // batch: every load of a batch is issued before any is used, so a batch
-    // costs one memory round trip
+    // costs one memory round trip; then, per destination, the lane appends
+    // the receive row to its own list and two warp reductions give the
+    // chunk's first and last window slot (the notice)
     for (int d00 = 0; d00 < R; d00 += 4 * kMetaLoads) {
         int4 q[kMetaLoads];
 #pragma unroll
@@ -593,15 +600,116 @@ __device__ void build_meta(const DispatchParams &p, int k, const MetaSlot &ms, c
     if (lane == 31) ms.pref[32] = incl;
 }
 
+__device__ void build_meta_by_dest(const DispatchParams &p, int k, const MetaSlot &ms, const int *rbase) {
+    const int lane = threadIdx.x & 31;
+    const int R = p.R;
+    const int ntok = chunk_ntok(p, k);
+    const int64_t tok0 = chunk_tok0(p, k);
+    int32_t *notice = p.dev.notice + static_cast<int64_t>(k) * 2 * R;
+    int *buf = ms.dst;   // [32 x R]: the chunk's token_slot rows, then each token's receive rows
+    // 1. lane = token: its token_slot row (kMetaLoads x 4 destinations per
+    //    batch, every load of a batch issued before the first is stored)
+    {
+        const bool valid = lane < ntok;
+        const int64_t t = tok0 + lane;
+        int *row = buf + lane * R;
+        for (int d00 = 0; d00 < R; d00 += 4 * kMetaLoads) {
+            int4 q[kMetaLoads];
+#pragma unroll
+            for (int b = 0; b < kMetaLoads; ++b) {
+                const int d0 = d00 + 4 * b;
+                q[b] = make_int4(-1, -1, -1, -1);
+                if (valid && d0 < R) {
+                    if (p.slot_vec) {
+                        q[b] = __ldg(reinterpret_cast<const int4 *>(p.token_slot + t * R + d0));
+                    } else {
+                        if (d0 + 0 < R) q[b].x = __ldg(p.token_slot + t * R + d0 + 0);
+                        if (d0 + 1 < R) q[b].y = __ldg(p.token_slot + t * R + d0 + 1);
+                        if (d0 + 2 < R) q[b].z = __ldg(p.token_slot + t * R + d0 + 2);
+                        if (d0 + 3 < R) q[b].w = __ldg(p.token_slot + t * R + d0 + 3);
+                    }
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kMetaLoads; ++b) {
+                const int d0 = d00 + 4 * b;
+                if (d0 + 0 < R) row[d0 + 0] = q[b].x;
+                if (d0 + 1 < R) row[d0 + 1] = q[b].y;
+                if (d0 + 2 < R) row[d0 + 2] = q[b].z;
+                if (d0 + 3 < R) row[d0 + 3] = q[b].w;
+            }
+        }
+    }
+    __syncwarp();
+    // 2. lane = destination: per token, one ballot places the destination in
+    //    the token's list (token j's rows in increasing destination order,
+    //    written over its staged slots: a row lands at or before the slot it
+    //    came from, after every lane has read that slot); lane j keeps token
+    //    j's count.  The first and last window slots of the chunk per
+    //    destination are the notice.
+    const unsigned lt = (1u << lane) - 1u;
+    int mine = 0;   // lane j: receive rows listed for token j
+    for (int g = 0; g * 32 < R; ++g) {
+        const int d = g * 32 + lane;
+        const bool dv = d < R;
+        const int64_t rb = dv ? rbase[d] : 0;
+        int lo = -1, hi = -1;
+#pragma unroll 4
+        for (int j = 0; j < ntok; ++j) {
+            const int v = dv ? buf[j * R + d] : -1;
+            const bool member = v >= 0;
+            const unsigned bal = __ballot_sync(kFull, member);
+            const int cj = g > 0 ? __shfl_sync(kFull, mine, j) : 0;
+            if (member) {
+                const int64_t r = rb + v;
+                if (r >= 0 && r < p.cap_rows) {
+                    buf[j * R + cj + __popc(bal & lt)] = static_cast<int>(r);
+                } else {
+                    set_error(p.dev.err, EP_ERR_CAPACITY);
+                }
+                if (lo < 0) lo = v;
+                hi = v;
+            }
+            if (lane == j) mine += __popc(bal);
+        }
+        if (dv) *reinterpret_cast<int2 *>(notice + 2 * d) = make_int2(lo, hi);
+    }
+    // 3. list starts: exclusive prefix of the tokens' list lengths
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    ms.pref[lane] = incl - mine;
+    if (lane == 31) ms.pref[32] = incl;
+}
+
+// The chunk's destination lists (MetaSlot: per token, its receive rows in
+// increasing destination order; pref: where each token's list starts in the
+// chunk's sequence of (row, destination) pairs) and its notice (the first
+// and last window slot per destination rank).  Two equivalent builders: by
+// destination for chunks of up to 8 tokens -- a few ballots, and short, which
+// matters because the first chunk's lists hold up every copy CTA's first
+// stores -- and by token for larger chunks, where it measured faster.
+__device__ void build_meta(const DispatchParams &p, int k, const MetaSlot &ms, const int *rbase) {
+    if (chunk_ntok(p, k) <= 8)
+        build_meta_by_dest(p, k, ms, rbase);
+    else
+        build_meta_by_token(p, k, ms, rbase);
+}
+
 __device__ void meta_warp(const DispatchParams &p, uint8_t *smem, const SmemLayout &L, const Bars &bars,
                           const int *rbase, unsigned long long *words, const int *ids) {
     const int lane = threadIdx.x & 31;
     for (int m = 0;; ++m) {
         // chunk id m, once the copy warp has drawn it
         const uint64_t t0 = globaltimer_ns();
+        ErrPoll ep(t0);
         bool ok = true;
         while (ld_acquire_cta_shared(&words[kWIds]) <= static_cast<unsigned long long>(m)) {
-            if (read_error(p.dev.err) != 0 || globaltimer_ns() - t0 > p.timeout_ns) {
+            const uint64_t now = globaltimer_ns();
+            if (ep.raised(p.dev.err, now) || now - t0 > p.timeout_ns) {
                 ok = false;
                 break;
             }
@@ -634,6 +742,7 @@ __device__ void notify_warp(const DispatchParams &p, unsigned long long *words, 
     const unsigned int tag = static_cast<unsigned int>(words[kWGen]) + 1u;
     int done = 0;
     uint64_t idle_since = globaltimer_ns();
+    ErrPoll ep(idle_since);
     unsigned sleep = 32;
     while (true) {
         const int now = static_cast<int>(ld_acquire_cta_shared(&words[kWProgress]));
@@ -647,8 +756,9 @@ __device__ void notify_warp(const DispatchParams &p, unsigned long long *words, 
         }
         const unsigned long long fin = ld_acquire_cta_shared(&words[kWCopyDone]);
         if (fin != 0ull && static_cast<int>(ld_acquire_cta_shared(&words[kWProgress])) == done) break;
-        if (read_error(p.dev.err) != 0) break;
-        if (globaltimer_ns() - idle_since > p.timeout_ns) {
+        const uint64_t tnow = globaltimer_ns();
+        if (ep.raised(p.dev.err, tnow)) break;
+        if (tnow - idle_since > p.timeout_ns) {
             set_error(p.dev.err, EP_ERR_TIMEOUT);
             break;
         }
@@ -732,6 +842,7 @@ __device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long
         // answers the ring at once.
         bool pending = k < p.k1;          // this lane's chunk is not yet posted
         const uint64_t tw = globaltimer_ns();
+        ErrPoll ep(tw);
         while (__any_sync(kFull, pending) && !failed) {
             bool take_now = false;
             {
@@ -739,8 +850,8 @@ __device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long
                 while (true) {
                     if (pending && !take_now) take_now = ld_acquire_u32(p.dev.ready + k) == tag;
                     if (__any_sync(kFull, take_now)) break;
-                    const bool give_up =
-                        pending && (read_error(p.dev.err) != 0 || globaltimer_ns() - tw > p.timeout_ns);
+                    const uint64_t now = globaltimer_ns();
+                    const bool give_up = (lane == 0 && ep.raised(p.dev.err, now)) || (pending && now - tw > p.timeout_ns);
                     if (__any_sync(kFull, give_up)) {
                         if (read_error(p.dev.err) == 0) set_error(p.dev.err, EP_ERR_TIMEOUT);
                         failed = true;
@@ -1074,7 +1185,13 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
     const bool channel_cta = static_cast<int>(blockIdx.x) < p.C;
 
     // Prologue: barriers, window starts, and the checks every CTA takes alike
-    // so that either all of them run or none does.
+    // so that either all of them run or none does.  Per-channel message
+    // counts (for each ring's drain and the log capacity check) are summed by
+    // every thread at once into shared counters: one round of loads, not a
+    // dependent load per channel and destination.
+    unsigned *chan = reinterpret_cast<unsigned *>(smem + L.meta_off);   // [C], prologue only
+    long long n_recv = 0;
+    if (threadIdx.x < p.C) chan[threadIdx.x] = 0u;
     if (warp == 0 && lane == 0) {
         if (!channel_cta) {
             const int store_warps = p.vec_store ? p.store_warps : 1;
@@ -1089,7 +1206,9 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
             mbar_fence_init();
         }
         for (int i = 0; i < kNumWords; ++i) words[i] = 0ull;
+        const int rb_last = __ldg(p.recv_base + p.R - 1), rc_last = __ldg(p.recv_count + p.R - 1);
         words[kWGen] = ld_relaxed_u32(p.dev.disp_gen);
+        n_recv = static_cast<long long>(rb_last) + rc_last;
         if (channel_cta) {
             // the ring is drained between calls, so tail is where this call starts
             const unsigned long long base = ld_relaxed(p.dev.tail + static_cast<int64_t>(blockIdx.x) * kHeadStride);
@@ -1099,33 +1218,8 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
             words[kWLogged] = base;
         }
     }
-    if (warp == 1) {
+    if (warp == 1)
         for (int d = lane; d < p.R; d += 32) rbase[d] = __ldg(p.recv_base + d);
-        // N against the receive capacity; every channel's count against its log
-        const long long n_recv = static_cast<long long>(__ldg(p.recv_base + p.R - 1)) + __ldg(p.recv_count + p.R - 1);
-        long long worst = 0, mine = 0;
-        for (int c = 0; c < p.C; ++c) {
-            long long part = 0;
-            for (int d = c; d < p.R; d += p.C)
-                for (int s = p.s0 + lane; s < p.s1; s += 32) part += __ldg(p.msg_count + s * p.R + d);
-            for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
-            worst = max(worst, part);
-            if (channel_cta && c == static_cast<int>(blockIdx.x)) mine = part;
-        }
-        if (lane == 0) {
-            int abort = read_error(p.dev.err) != 0;
-            if (n_recv > p.cap_rows || n_recv < 0) {
-                set_error(p.dev.err, EP_ERR_CAPACITY);
-                abort = 1;
-            }
-            if (worst > p.log_cap) {
-                set_error(p.dev.err, EP_ERR_INVALID_ARG);
-                abort = 1;
-            }
-            words[kWAbort] = static_cast<unsigned long long>(abort);
-            words[kWExpected] = static_cast<unsigned long long>(mine);
-        }
-    }
     if (channel_cta) {
         // the ring: tags are laps of the cumulative index, so clear the slots
         // (a fresh launch's shared memory holds anything)
@@ -1138,6 +1232,36 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
             tab[RR + i] = __ldg(p.recv_off + i);
             tab[2 * RR + i] = __ldg(p.send_off + i);
         }
+    }
+    __syncthreads();
+    {
+        const int npairs = (p.s1 - p.s0) * p.R;
+        const int32_t *mc = p.msg_count + static_cast<int64_t>(p.s0) * p.R;
+        for (int i0 = threadIdx.x; i0 < npairs; i0 += 4 * kThreads) {
+            int v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v[q] = i0 + q * kThreads < npairs ? __ldg(mc + i0 + q * kThreads) : 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (v[q] != 0) atomicAdd(&chan[((i0 + q * kThreads) % p.R) % p.C], static_cast<unsigned>(v[q]));
+        }
+    }
+    __syncthreads();
+    if (warp == 0 && lane == 0) {
+        // N against the receive capacity; every channel's count against its log
+        long long worst = 0;
+        for (int c = 0; c < p.C; ++c) worst = max(worst, static_cast<long long>(chan[c]));
+        int abort = read_error(p.dev.err) != 0;
+        if (n_recv > p.cap_rows || n_recv < 0) {
+            set_error(p.dev.err, EP_ERR_CAPACITY);
+            abort = 1;
+        }
+        if (worst > p.log_cap) {
+            set_error(p.dev.err, EP_ERR_INVALID_ARG);
+            abort = 1;
+        }
+        words[kWAbort] = static_cast<unsigned long long>(abort);
+        words[kWExpected] = channel_cta ? static_cast<unsigned long long>(chan[blockIdx.x]) : 0ull;
     }
     __syncthreads();
     const long long expected = static_cast<long long>(words[kWExpected]);

@@ -339,16 +339,33 @@ __device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Reads a grid's error word at most once per kErrPollNs.  Waiting warps of
+// every CTA poll it; read on every spin, that one word became the hottest
+// line in L2 and slowed every access that shared its slice.
+constexpr uint64_t kErrPollNs = 10000;
+struct ErrPoll {
+    uint64_t next;
+    __device__ __forceinline__ explicit ErrPoll(uint64_t now) : next(now + kErrPollNs) {}
+    __device__ __forceinline__ bool raised(const int32_t *err, uint64_t now) {
+        if (now < next) return false;
+        next = now + kErrPollNs;
+        return read_error(err) != 0;
+    }
+};
+
 // Bounded wait: true when the phase completed; false when the time limit ran
-// out or (err != nullptr) another thread of the grid already raised an error.
+// out or (err != nullptr) another thread of the grid raised an error (seen
+// within kErrPollNs).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, const int32_t *err,
                                                   uint64_t timeout_ns) {
     if (mbar_try(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    ErrPoll ep(t0);
     while (true) {
         if (mbar_try(bar, parity)) return true;
-        if (err != nullptr && read_error(err) != 0) return false;
-        if (globaltimer_ns() - t0 > timeout_ns) return false;
+        const uint64_t now = globaltimer_ns();
+        if (err != nullptr && ep.raised(err, now)) return false;
+        if (now - t0 > timeout_ns) return false;
     }
 }
 
