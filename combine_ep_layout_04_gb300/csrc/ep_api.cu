@@ -225,6 +225,10 @@ ep_status ep_create(const ep_config *cfg, ep_handle *out) {
     const size_t o_signal = cv.take<unsigned long long>(R);
     const size_t o_xticket = cv.take<unsigned long long>(1);
     const size_t o_xdesc = cv.take<unsigned long long>(static_cast<size_t>(h->xtiles) * E);
+    // rows landed per multi-row message that spans chunks, indexed by its first
+    // send row (N <= T * min(K, R)); only messages of G > 1 rows span chunks
+    const int64_t kmin_all = cfg->topk < R ? cfg->topk : R;
+    const size_t o_msgrows = cv.take<unsigned int>(h->G > 1 ? static_cast<size_t>(T * kmin_all) : 0);
     h->alloc_bytes = cv.off;
     if (cudaMalloc(&h->alloc_base, h->alloc_bytes) != cudaSuccess) {
         delete h;
@@ -257,6 +261,7 @@ ep_status ep_create(const ep_config *cfg, ep_handle *out) {
     d.signal = reinterpret_cast<unsigned long long *>(b + o_signal);
     d.xticket = reinterpret_cast<unsigned long long *>(b + o_xticket);
     d.xdesc = reinterpret_cast<unsigned long long *>(b + o_xdesc);
+    d.msg_rows = reinterpret_cast<unsigned int *>(b + o_msgrows);
     if (cudaDeviceSynchronize() != cudaSuccess) {
         cudaFree(h->alloc_base);
         delete h;

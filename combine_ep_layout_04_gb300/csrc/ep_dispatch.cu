@@ -94,16 +94,19 @@ constexpr int kNoticeLoads = 8;           // notice entries a poster lane keeps 
 // ring tail = retire point (channel CTA); poller stopped; ring base; dispatch
 // generation; messages expected on the channel; ring head; records logged;
 // chunk ids drawn (copy CTA); chunks stored in all, once known (copy CTA);
-// items loaded in all + 1, once known (copy CTA, vector-store path).
+// items loaded in all + 1, once known (copy CTA, vector-store path); chunks
+// flagged by the notify warp (copy CTA); message counters in shared memory
+// + 1, or 0 when they live in device memory (channel CTA, G > 1).
 // Then, in copy CTAs, the drawn chunk ids (a ring of kIdSlots ints) and, per
 // stage, the description of the item it holds (vector-store path).
 enum {
     kWAbort = 0, kWProgress = 1, kWStopped = 2, kWBase = 3, kWGen = 4, kWExpected = 5, kWHead = 6, kWLogged = 7,
-    kWIds = 8, kWCopyDone = 9, kWItems = 10
+    kWIds = 8, kWCopyDone = 9, kWItems = 10, kWNotified = 11, kWCounters = 12
 };
-constexpr int kNumWords = 11;
+constexpr int kNumWords = 13;
 constexpr int kIdSlots = 32;   // chunk ids a copy CTA has drawn but not yet retired
 constexpr int kStagesMax = 15;
+constexpr int kSmallPerCta = 6;   // small chunks per copy CTA at the end of a layer
 
 // Rows of at most kVecRowMax bytes leave shared memory by vector stores from
 // the copy CTA's store warps (warps kStoreWarp0..) instead of TMA bulk
@@ -124,6 +127,12 @@ struct SmemLayout {
         return (ranges_off(R, D) + npw * ranges_bytes_per_warp(R, C) + 15) & ~15;
     }
     static constexpr int kListBytesPerWarp = 32 * kListPerLane * 16;
+    // message counters (G > 1): per (source, destination of the ring) the
+    // first counter of the pair's messages, then one counter per message; in
+    // the space below meta_off that copy CTAs give to stages
+    __host__ __device__ static int counters_off(int R, int C, int D, int npw) {
+        return (lists_off(R, C, D, npw) + npw * kListBytesPerWarp + 15) & ~15;
+    }
     // npw: the poster warps that run (fewer when their ranges would not fit
     // beside the ring, e.g. 64 destinations on one channel)
     __host__ __device__ SmemLayout(int R, int C, int D, int stage_bytes, int stages, int npw) {
@@ -153,13 +162,38 @@ struct MetaSlot {
 };
 
 
-__device__ __forceinline__ int chunk_ntok(const DispatchParams &p, int k) {
-    const int ci = k % p.chunks_per_rank;
-    return min(p.chunk_tokens, p.Tpr - ci * p.chunk_tokens);
+// Chunk geometry (see DispatchParams): source rank, first token and tokens
+// of chunk k; the chunk before it in its rank's token order (or -1); and the
+// call's u-th chunk in draw order.
+__device__ __forceinline__ int chunk_src(const DispatchParams &p, int k) {
+    const int rb = p.R * p.nbig;
+    return k < rb ? k / p.nbig : (k - rb) / p.nsmall;
 }
 __device__ __forceinline__ int64_t chunk_tok0(const DispatchParams &p, int k) {
-    const int s = k / p.chunks_per_rank, ci = k % p.chunks_per_rank;
-    return static_cast<int64_t>(s) * p.Tpr + static_cast<int64_t>(ci) * p.chunk_tokens;
+    const int rb = p.R * p.nbig;
+    if (k < rb) {
+        const int s = k / p.nbig, i = k - s * p.nbig;
+        return static_cast<int64_t>(s) * p.Tpr + static_cast<int64_t>(i) * p.chunk_tokens;
+    }
+    const int k2 = k - rb, s = k2 / p.nsmall, j = k2 - s * p.nsmall;
+    return static_cast<int64_t>(s) * p.Tpr + static_cast<int64_t>(p.nbig) * p.chunk_tokens +
+           static_cast<int64_t>(j) * p.small_tokens;
+}
+__device__ __forceinline__ int chunk_ntok(const DispatchParams &p, int k) {
+    const int rb = p.R * p.nbig;
+    if (k < rb) return p.chunk_tokens;
+    const int j = (k - rb) % p.nsmall;
+    return min(p.small_tokens, p.Tpr - p.nbig * p.chunk_tokens - j * p.small_tokens);
+}
+__device__ __forceinline__ int chunk_pred(const DispatchParams &p, int k) {
+    const int rb = p.R * p.nbig;
+    if (k < rb) return k % p.nbig != 0 ? k - 1 : -1;
+    const int k2 = k - rb, s = k2 / p.nsmall, j = k2 - s * p.nsmall;
+    return j != 0 ? k - 1 : (p.nbig > 0 ? s * p.nbig + p.nbig - 1 : -1);
+}
+__device__ __forceinline__ int call_chunk(const DispatchParams &p, int u) {
+    const int nb_call = (p.s1 - p.s0) * p.nbig;
+    return u < nb_call ? p.s0 * p.nbig + u : p.R * p.nbig + p.s0 * p.nsmall + (u - nb_call);
 }
 __device__ __forceinline__ int chunk_items(const DispatchParams &p, int ntok) {
     return p.pieces > 1 ? ntok * p.pieces : (ntok + p.rows_per_item - 1) / p.rows_per_item;
@@ -203,7 +237,8 @@ struct Bars {
 };
 
 // The chunks a copy CTA copies, in order: its first is fixed (copy CTA i
-// takes chunk i of the call), the rest come from a device-wide counter, so
+// takes the call's chunk i in draw order), the rest come from a device-wide
+// counter, so
 // that CTAs on faster SMs take more and all finish together.  Each draw
 // publishes the chunk id to the CTA's other warps first and only then asks
 // the counter for the next one, so that the atomic's round trip overlaps a
@@ -221,7 +256,22 @@ struct ChunkDraw {
         const unsigned ncopy = gridDim.x - static_cast<unsigned>(p.C);
         int k = -1;
         if (lane == 0) {
-            k = ahead < static_cast<unsigned>(p.k1 - p.k0) ? p.k0 + static_cast<int>(ahead) : -1;
+            // the ring of ids holds kIdSlots chunks: wait until the notify
+            // warp is done with the one this draw replaces
+            if (n_drawn >= kIdSlots) {
+                const uint64_t t0 = globaltimer_ns();
+                ErrPoll ep(t0);
+                while (ld_acquire_cta_shared(&words[kWNotified]) <= static_cast<unsigned long long>(n_drawn - kIdSlots)) {
+                    const uint64_t tn = globaltimer_ns();
+                    if (ep.raised(p.dev.err, tn) || tn - t0 > p.timeout_ns) {
+                        if (read_error(p.dev.err) == 0) set_error(p.dev.err, EP_ERR_TIMEOUT);
+                        ahead = static_cast<unsigned>(p.nk);   // draw nothing more
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+            }
+            k = ahead < static_cast<unsigned>(p.nk) ? call_chunk(p, static_cast<int>(ahead)) : -1;
             ids[n_drawn % kIdSlots] = k;
         }
         k = __shfl_sync(kFull, k, 0);
@@ -750,6 +800,7 @@ __device__ void notify_warp(const DispatchParams &p, unsigned long long *words, 
             fence_acq_rel_gpu();   // the chunks' rows are visible device-wide before their flags
             for (int m = done; m < now; ++m) st_relaxed_u32(p.dev.ready + ids[m % kIdSlots], tag);
             done = now;
+            st_release_cta_shared(&words[kWNotified], static_cast<unsigned long long>(done));
             idle_since = globaltimer_ns();
             sleep = 32;
             continue;
@@ -818,10 +869,14 @@ static_assert(kThreads / 32 == kPosterWarps + 2, "one warp per poster, plus the 
 __device__ __forceinline__ int poster_index(int warp) { return warp - (warp > kPollWarp) - (warp > kLogWarp); }
 
 __device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long long *words, const PairTables &pt,
-                            unsigned long long *ring, int2 *ranges, unsigned long long *list) {
+                            unsigned long long *ring, int2 *ranges, unsigned long long *list, int *msgoff) {
     const int lane = threadIdx.x & 31;
     const int R = p.R, C = p.C, G = p.G;
     const int nd = c < R ? (R - 1 - c) / C + 1 : 0;   // destinations d = c, c + C, ... on this ring
+    // message counters for G > 1: in shared memory when they fit (msgoff
+    // gives each pair's first), else in device memory at each message's
+    // first send row
+    unsigned *ctr_smem = (G > 1 && words[kWCounters] != 0ull) ? reinterpret_cast<unsigned *>(msgoff) + R * nd : nullptr;
     const int ndmax = (R + C - 1) / C;
     const unsigned long long dmask = static_cast<unsigned long long>(p.D - 1);
     const unsigned long long limit = static_cast<unsigned long long>(p.max_inflight);
@@ -831,16 +886,17 @@ __device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long
     const int leader = (lane / p.batch) * p.batch;    // first lane of this lane's batch
     LaneStats st;
     bool failed = false;
-    const int ngroups = nd > 0 ? (p.k1 - p.k0 + 31) / 32 : 0;
+    const int ngroups = nd > 0 ? (p.nk + 31) / 32 : 0;
     uint64_t err_checked = globaltimer_ns();
     for (int grp = w; grp < ngroups && !failed; grp += p.poster_warps) {
-        const int k = p.k0 + grp * 32 + lane;
+        const int u = grp * 32 + lane;   // this lane's chunk: the call's u-th
+        const int k = u < p.nk ? call_chunk(p, u) : -1;
         // Post the group's chunks as they become ready: wait until at least
         // one pending chunk's flag is set (polling device memory with a
         // back-off), post every chunk found ready, and come back for the
         // rest.  While posting, the warp touches shared memory only and
         // answers the ring at once.
-        bool pending = k < p.k1;          // this lane's chunk is not yet posted
+        bool pending = u < p.nk;          // this lane's chunk is not yet posted
         const uint64_t tw = globaltimer_ns();
         ErrPoll ep(tw);
         while (__any_sync(kFull, pending) && !failed) {
@@ -868,7 +924,7 @@ __device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long
             {
                 bool bad = false;
                 if (take_now) {
-                    const int s = k / p.chunks_per_rank;
+                    const int s = chunk_src(p, k);
                     const int32_t *nt = p.dev.notice + static_cast<int64_t>(k) * 2 * R;
                     // kNoticeLoads destinations' notices in flight at once
                     int2 lhs[kNoticeLoads];
@@ -891,8 +947,43 @@ __device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long
                             if (jlo < 0 || jhi < jlo || jhi >= cnt) {
                                 bad = true;
                             } else {
-                                gb = jlo / G;
-                                ge = max(gb, (jhi == cnt - 1) ? (cnt - 1) / G + 1 : (jhi + 1) / G);
+                                // messages g in [ga, gz] have rows here; message g
+                                // is rows [gG, min(gG + G, cnt)) of the pair
+                                const int ga = jlo / G, gz = jhi / G;
+                                gb = ga;
+                                ge = gz + 1;
+                                if (G > 1) {
+                                    // a message with rows outside this chunk is posted
+                                    // by whichever of its chunks lands last: each adds
+                                    // the rows it holds to the message's counter
+                                    const int za = ga * G, zz = gz * G;
+                                    const int enda = min(za + G, cnt) - 1, endz = min(zz + G, cnt) - 1;
+                                    // true when these rows complete message g (its counter
+                                    // is left at zero for the next call)
+                                    auto lands = [&](int g, int z, unsigned rows, int size) -> bool {
+                                        if (ctr_smem != nullptr) {
+                                            unsigned *q = ctr_smem + msgoff[s * nd + i] + g;
+                                            if (atom_add_acq_rel_cta_shared(q, rows) + rows != static_cast<unsigned>(size))
+                                                return false;
+                                            *q = 0u;
+                                        } else {
+                                            unsigned *q = p.msg_rows + pt.send0[s * R + d] + z;
+                                            if (atom_add_acq_rel(q, rows) + rows != static_cast<unsigned>(size)) return false;
+                                            *q = 0u;
+                                        }
+                                        return true;
+                                    };
+                                    if (ga == gz) {
+                                        if ((za < jlo || enda > jhi) &&
+                                            !lands(ga, za, static_cast<unsigned>(jhi - jlo + 1), enda - za + 1))
+                                            ge = gb;
+                                    } else {
+                                        if (za < jlo && !lands(ga, za, static_cast<unsigned>(enda - jlo + 1), enda - za + 1))
+                                            gb = ga + 1;
+                                        if (endz > jhi && !lands(gz, zz, static_cast<unsigned>(jhi - zz + 1), endz - zz + 1))
+                                            ge = gz;
+                                    }
+                                }
                             }
                         }
                         ranges[lane * ndmax + i] = make_int2(gb, ge);
@@ -911,7 +1002,7 @@ __device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long
             // a round, one command per lane.  A batch may span chunks.
             int left = total;            // this lane's commands not yet listed
             int ci = 0, cm = 0;          // cursor: destination index, message past gb
-            const int s_lane = take_now ? k / p.chunks_per_rank : 0;
+            const int s_lane = take_now ? chunk_src(p, k) : 0;
             while (!failed) {
                 const int take = min(left, kListPerLane);
                 int incl = take;
@@ -1263,7 +1354,43 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
         words[kWAbort] = static_cast<unsigned long long>(abort);
         words[kWExpected] = channel_cta ? static_cast<unsigned long long>(chan[blockIdx.x]) : 0ull;
     }
+    if (channel_cta && p.G > 1 && warp == 1) {
+        // message counters of this ring: the first one of each pair (s, d),
+        // d = c + i*C, in (s, i) order; shared memory if they fit, else the
+        // device-memory counters are used
+        const int c = blockIdx.x;
+        const int nd = c < p.R ? (p.R - 1 - c) / p.C + 1 : 0;
+        int *msgoff = reinterpret_cast<int *>(smem + SmemLayout::counters_off(p.R, p.C, p.D, p.poster_warps));
+        const int *cntt = reinterpret_cast<const int *>(smem);
+        int run = 0;
+        for (int b0 = 0; b0 < p.R * nd; b0 += 32) {
+            const int idx = b0 + lane;
+            int m = 0;
+            if (idx < p.R * nd) {
+                const int sr = idx / nd, i = idx - sr * nd;
+                m = (cntt[sr * p.R + c + i * p.C] + p.G - 1) / p.G;
+            }
+            int incl = m;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (idx < p.R * nd) msgoff[idx] = run + incl - m;
+            run += __shfl_sync(kFull, incl, 31);
+        }
+        const long long room = (L.meta_off - SmemLayout::counters_off(p.R, p.C, p.D, p.poster_warps)) / 4 - p.R * nd;
+        if (lane == 0) words[kWCounters] = run <= room ? static_cast<unsigned long long>(run) + 1ull : 0ull;
+    }
     __syncthreads();
+    if (channel_cta && p.G > 1 && words[kWCounters] != 0ull) {
+        const int nd = static_cast<int>(blockIdx.x) < p.R ? (p.R - 1 - static_cast<int>(blockIdx.x)) / p.C + 1 : 0;
+        unsigned *ctr = reinterpret_cast<unsigned *>(smem + SmemLayout::counters_off(p.R, p.C, p.D, p.poster_warps)) +
+                        p.R * nd;
+        const int n = static_cast<int>(words[kWCounters] - 1ull);
+        for (int i = threadIdx.x; i < n; i += blockDim.x) ctr[i] = 0u;
+        __syncthreads();
+    }
     const long long expected = static_cast<long long>(words[kWExpected]);
 
     if (words[kWAbort] == 0ull) {
@@ -1280,7 +1407,8 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
                     smem + SmemLayout::lists_off(p.R, p.C, p.D, p.poster_warps) + pw * SmemLayout::kListBytesPerWarp;
                 if (pw < p.poster_warps)
                 poster_warp(p, c, pw, words, pt, reinterpret_cast<unsigned long long *>(smem + SmemLayout::ring_off(p.R)),
-                            reinterpret_cast<int2 *>(rb), reinterpret_cast<unsigned long long *>(lb));
+                            reinterpret_cast<int2 *>(rb), reinterpret_cast<unsigned long long *>(lb),
+                            reinterpret_cast<int *>(smem + SmemLayout::counters_off(p.R, p.C, p.D, p.poster_warps)));
             } else if (!(p.debug & EP_DEBUG_DISABLE_CONSUMER)) {
                 unsigned long long *ring = reinterpret_cast<unsigned long long *>(smem + SmemLayout::ring_off(p.R));
                 unsigned long long *stage = ring + 2 * p.D;
@@ -1375,8 +1503,20 @@ ep_status plan_dispatch(ep_ctx *h) {
     h->disp_smem = static_cast<size_t>(L.total);
     h->disp_threads = kThreads;
     h->chunk_tokens = chunk_tokens;
-    h->chunks_per_rank = (h->cfg.tokens_per_rank + chunk_tokens - 1) / chunk_tokens;
-    h->nchunks = h->chunks_per_rank * R;
+    // With big chunks of 16 tokens or more on the TMA path, the last tokens of
+    // every rank go in small chunks (a quarter of the big size), about
+    // kSmallPerCta of them per copy CTA over the layer: they are drawn last,
+    // so the copy CTAs finish within a small chunk of each other.  (Measured
+    // slower elsewhere: 1-token chunks, and 8-token chunks of small rows.)
+    const int Tpr = h->cfg.tokens_per_rank;
+    const bool tiers = chunk_tokens >= 16 && B > kVecRowMax;
+    const int small_tokens = tiers ? chunk_tokens / 4 : chunk_tokens;
+    const int64_t tail_target = tiers ? (static_cast<int64_t>(kSmallPerCta) * copy_ctas * small_tokens + R - 1) / R : 0;
+    const int big_tok = Tpr > tail_target ? static_cast<int>((Tpr - tail_target) / chunk_tokens) * chunk_tokens : 0;
+    h->small_tokens = small_tokens;
+    h->nbig = big_tok / chunk_tokens;
+    h->nsmall = (Tpr - big_tok + small_tokens - 1) / small_tokens;
+    h->nchunks = (h->nbig + h->nsmall) * R;
     if (cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(h->disp_smem)) != cudaSuccess)
         return EP_ERR_CUDA;
@@ -1415,13 +1555,15 @@ ep_status launch_dispatch(ep_ctx *h, const void *x, const ep_layout_out *lay, vo
     p.G = h->G;
     p.drain_batch = h->cfg.drain_batch;
     p.debug = h->cfg.debug_flags;
-    p.chunks_per_rank = h->chunks_per_rank;
+    p.msg_rows = h->dev.msg_rows;
+    p.nbig = h->nbig;
+    p.nsmall = h->nsmall;
+    p.small_tokens = h->small_tokens;
     p.chunk_tokens = h->chunk_tokens;
     p.nchunks = h->nchunks;
     p.s0 = s_begin;
     p.s1 = s_end;
-    p.k0 = s_begin * h->chunks_per_rank;
-    p.k1 = s_end * h->chunks_per_rank;
+    p.nk = (s_end - s_begin) * (h->nbig + h->nsmall);
     p.rows_per_item = h->rows_per_item;
     p.pieces = h->pieces;
     p.piece_bytes = h->piece_bytes;

@@ -52,6 +52,8 @@ struct DevState {
     unsigned int *disp_done;            // CTAs finished in the current dispatch
     unsigned int *chunk_next;           // next chunk to hand to a copy CTA in the current dispatch
     unsigned long long *signal;         // [R] messages landed per destination rank (cumulative)
+    unsigned int *msg_rows;             // [T * min(K, R)] when G > 1: rows landed of a message that
+                                        // spans chunks, at its first send row; zero between calls
     // expert layout scan
     unsigned long long *xticket;        // expert-layout tiles handed out so far (all calls)
     unsigned long long *xdesc;          // [xtiles * E] packed (epoch, flag, value)
@@ -78,15 +80,20 @@ struct DispatchParams {
     int64_t cap_rows;
     const int32_t *token_slot, *recv_base, *recv_count, *recv_off, *send_off, *cnt, *msg_count;
     DevState dev;
+    unsigned int *msg_rows;   // dev.msg_rows (G > 1)
     int64_t T;
     int64_t row_bytes;
     int64_t log_cap;
     uint64_t timeout_ns;
     int R, Tpr, C, D, max_inflight, batch, G, drain_batch, debug;
-    int chunks_per_rank, nchunks;
-    int k0, k1;          // chunks of this call: those of source ranks [s0, s1)
+    // A source rank's tokens are cut into nbig chunks of chunk_tokens tokens,
+    // then nsmall chunks of small_tokens (the last may be short).  Chunk ids:
+    // big chunks rank-major [0, R*nbig), then small chunks rank-major; a call
+    // draws its big chunks first, so the last work handed out is fine-grained.
+    int nbig, nsmall, small_tokens, nchunks;
+    int nk;              // chunks of this call: those of source ranks [s0, s1)
     int s0, s1;
-    int chunk_tokens;    // tokens per chunk (4..32)
+    int chunk_tokens;    // tokens per big chunk (4..32)
     int rows_per_item;   // tokens per item when a row fits a stage, else 1
     int pieces;          // pieces per row when it does not, else 1
     int piece_bytes;     // bytes per piece (a multiple of 16)
@@ -133,7 +140,7 @@ struct ep_ctx {
     size_t disp_smem;
     int stage_bytes, stages, prefetch, meta_slots, store_lag;
     int rows_per_item, pieces, piece_bytes;
-    int chunks_per_rank, nchunks, chunk_tokens;
+    int nbig, nsmall, small_tokens, nchunks, chunk_tokens;
     int vec_store;
     int poster_warps;
     int64_t log_cap;
@@ -201,6 +208,20 @@ __device__ __forceinline__ void st_release(unsigned long long *p, unsigned long 
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// atomic add with acquire and release semantics (GPU scope); returns the old value
+__device__ __forceinline__ unsigned int atom_add_acq_rel(unsigned int *p, unsigned int v) {
+    unsigned int old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ unsigned int atom_add_acq_rel_cta_shared(unsigned int *p, unsigned int v) {
+    unsigned int old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(v)
+                 : "memory");
+    return old;
+}
 __device__ __forceinline__ void red_add_relaxed(unsigned long long *p, unsigned long long v) {
     asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
