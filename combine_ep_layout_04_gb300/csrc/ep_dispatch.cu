@@ -117,7 +117,7 @@ constexpr int kStoreWarp0 = 3;
 
 // Shared-memory carve, identical on host and device.
 struct SmemLayout {
-    int stage_off, meta_off, meta_slot_bytes, scratch_off, info_off, bar_off, total;
+    int stage_off, meta_off, meta_slot_bytes, scratch_off, info_off, chan_off, bar_off, total;
     __host__ __device__ static int ring_off(int R) { return ((12 * R * R) + 127) / 128 * 128; }
     // poster ranges: per poster warp, 32 chunks x ceil(R/C) int2
     __host__ __device__ static int ranges_off(int R, int D) { return ring_off(R) + 16 * D + 16 * kLogStage; }
@@ -147,7 +147,8 @@ struct SmemLayout {
         // scratch: rbase[R] ints, kNumWords u64 words, kIdSlots ints,
         // kStagesMax item descriptions (int4)
         info_off = (scratch_off + ((R + 3) & ~3) * 4 + 8 * kNumWords + 4 * kIdSlots + 15) & ~15;
-        bar_off = info_off + 16 * kStagesMax;
+        chan_off = info_off + 16 * kStagesMax;          // per-channel message counts (prologue)
+        bar_off = chan_off + 4 * kMaxChannels;
         // barriers: stage_full[stages], meta_full[3], meta_free[3], stage_empty[stages]
         total = bar_off + 8 * (2 * stages + 2 * kMetaSlots);
     }
@@ -1280,7 +1281,7 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
     // counts (for each ring's drain and the log capacity check) are summed by
     // every thread at once into shared counters: one round of loads, not a
     // dependent load per channel and destination.
-    unsigned *chan = reinterpret_cast<unsigned *>(smem + L.meta_off);   // [C], prologue only
+    unsigned *chan = reinterpret_cast<unsigned *>(smem + L.chan_off);   // [C], prologue only
     long long n_recv = 0;
     if (threadIdx.x < p.C) chan[threadIdx.x] = 0u;
     if (warp == 0 && lane == 0) {
@@ -1354,42 +1355,45 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
         words[kWAbort] = static_cast<unsigned long long>(abort);
         words[kWExpected] = channel_cta ? static_cast<unsigned long long>(chan[blockIdx.x]) : 0ull;
     }
-    if (channel_cta && p.G > 1 && warp == 1) {
-        // message counters of this ring: the first one of each pair (s, d),
-        // d = c + i*C, in (s, i) order; shared memory if they fit, else the
-        // device-memory counters are used
+    __syncthreads();
+    if (channel_cta && p.G > 1) {
+        // message counters of this ring: the first one of each
+        // pair (s, d), d = c + i*C, in (s, i) order, then one per message, in
+        // shared memory if they fit; else the device-memory counters are used
         const int c = blockIdx.x;
         const int nd = c < p.R ? (p.R - 1 - c) / p.C + 1 : 0;
-        int *msgoff = reinterpret_cast<int *>(smem + SmemLayout::counters_off(p.R, p.C, p.D, p.poster_warps));
-        const int *cntt = reinterpret_cast<const int *>(smem);
-        int run = 0;
-        for (int b0 = 0; b0 < p.R * nd; b0 += 32) {
-            const int idx = b0 + lane;
-            int m = 0;
-            if (idx < p.R * nd) {
-                const int sr = idx / nd, i = idx - sr * nd;
-                m = (cntt[sr * p.R + c + i * p.C] + p.G - 1) / p.G;
-            }
-            int incl = m;
+        const int coff = SmemLayout::counters_off(p.R, p.C, p.D, p.poster_warps);
+        const long long room = static_cast<long long>(L.meta_off - coff) / 4 - static_cast<long long>(p.R) * nd;
+        if (warp == 1) {
+            int *msgoff = reinterpret_cast<int *>(smem + coff);
+            const int *cntt = reinterpret_cast<const int *>(smem);
+            int run = 0;
+            for (int b0 = 0; room >= 0 && b0 < p.R * nd; b0 += 32) {
+                const int idx = b0 + lane;
+                int m = 0;
+                if (idx < p.R * nd) {
+                    const int sr = idx / nd, i = idx - sr * nd;
+                    m = (cntt[sr * p.R + c + i * p.C] + p.G - 1) / p.G;
+                }
+                int incl = m;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(kFull, incl, o);
-                if (lane >= o) incl += y;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(kFull, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                if (idx < p.R * nd) msgoff[idx] = run + incl - m;
+                run += __shfl_sync(kFull, incl, 31);
             }
-            if (idx < p.R * nd) msgoff[idx] = run + incl - m;
-            run += __shfl_sync(kFull, incl, 31);
+            if (lane == 0)
+                words[kWCounters] = room >= 0 && run <= room ? static_cast<unsigned long long>(run) + 1ull : 0ull;
         }
-        const long long room = (L.meta_off - SmemLayout::counters_off(p.R, p.C, p.D, p.poster_warps)) / 4 - p.R * nd;
-        if (lane == 0) words[kWCounters] = run <= room ? static_cast<unsigned long long>(run) + 1ull : 0ull;
-    }
-    __syncthreads();
-    if (channel_cta && p.G > 1 && words[kWCounters] != 0ull) {
-        const int nd = static_cast<int>(blockIdx.x) < p.R ? (p.R - 1 - static_cast<int>(blockIdx.x)) / p.C + 1 : 0;
-        unsigned *ctr = reinterpret_cast<unsigned *>(smem + SmemLayout::counters_off(p.R, p.C, p.D, p.poster_warps)) +
-                        p.R * nd;
-        const int n = static_cast<int>(words[kWCounters] - 1ull);
-        for (int i = threadIdx.x; i < n; i += blockDim.x) ctr[i] = 0u;
         __syncthreads();
+        if (words[kWCounters] != 0ull) {
+            unsigned *ctr = reinterpret_cast<unsigned *>(smem + coff) + p.R * nd;
+            const int n = static_cast<int>(words[kWCounters] - 1ull);
+            for (int i = threadIdx.x; i < n; i += blockDim.x) ctr[i] = 0u;
+            __syncthreads();
+        }
     }
     const long long expected = static_cast<long long>(words[kWExpected]);
 
