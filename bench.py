@@ -321,6 +321,8 @@ def main():
                          "sequential against pipelined on three streams")
     ap.add_argument("--sweep", choices=["msg"], default=None,
                     help="msg: dispatch bandwidth against row and message size, one JSON line per point")
+    ap.add_argument("--points", default=None,
+                    help="with --sweep: comma-separated point labels to run (e.g. latency,B1024_G4); default all")
     args = ap.parse_args()
     assert args.warmup >= 3 or os.environ.get("EP_BENCH_ALLOW_SHORT_WARMUP"), "warm-up must be >= 3 steps"
 
@@ -730,17 +732,22 @@ def run_overlap(args, w, pieces: int = 4, gemm_cols: int = 256, reps: int = 10):
 
 
 # --------------------------------------------------------------------- sweep
-SWEEP_ROW_BYTES = (1024, 2048, 4096, 7168, 8192, 14336, 28672, 57344)
+SWEEP_ROW_BYTES = (1024, 2048, 4096, 7168, 8192, 14336, 28672, 57344, 131072, 1048576)
 SWEEP_MSG_ROWS = (1, 4, 16, 64, 256, 1024)
 
 
 def sweep_points():
-    """(row bytes B, rows per message G) pairs: every row size at G = 1, the
-    packing threshold (4 KB and 7 KB rows at G = 1 and 8), and message sizes
-    from 1 KB to 16 MB at B = 1 KB and B = 16 KB."""
+    """(row bytes B, rows per message G) pairs: every row size at G = 1 (1 KB
+    to 1 MB rows), the packing threshold (4 KB and 7 KB rows at G = 1 and 8),
+    message sizes from 1 KB to 16 MB at B = 1 KB and B = 16 KB, and 2, 4, 8
+    and 16 MB messages of 8 KB rows (G up to 2047, the most a message holds)
+    and of 1 MB rows."""
     pts = [(b, 1) for b in SWEEP_ROW_BYTES]
     pts += [(b, 8) for b in (4096, 7168)]
     pts += [(b, g) for b in (1024, 16384) for g in SWEEP_MSG_ROWS if g > 1]
+    pts += [(8192, g) for g in (256, 512, 1024, 2047)]
+    pts += [(16384, g) for g in (128, 512)]
+    pts += [(1048576, 16)]
     return pts
 
 
@@ -768,6 +775,11 @@ def run_sweep(args):
         tpr = int(4 * 2**30 / (R * R * frac_dst * b))
         tpr = max(tpr, int(np.ceil(g / frac_dst)))
         cases.append((f"B{b}_G{g}", W.Workload(f"sweep-B{b}-G{g}", R, tpr, b // 2, E, K, seed=707), g))
+    if getattr(args, "points", None):
+        keep = set(args.points.split(","))
+        unknown = keep - {label for label, _, _ in cases}
+        assert not unknown, f"unknown sweep points: {sorted(unknown)}"
+        cases = [c for c in cases if c[0] in keep]
     for label, w, g in cases:
         idx, _ = W.make_routing(w)
         topk = torch.from_numpy(idx).to(dev)

@@ -17,6 +17,7 @@ EP_ERR_TIMEOUT = 3
 EP_ERR_CUDA = 4
 EP_ERR_NOT_READY = 5
 EP_DEBUG_DISABLE_CONSUMER = 0x1
+EP_DEBUG_DEVICE_COUNTERS = 0x2
 
 _STATUS_NAMES = {0: "EP_OK", 1: "EP_ERR_INVALID_ARG", 2: "EP_ERR_CAPACITY", 3: "EP_ERR_TIMEOUT",
                  4: "EP_ERR_CUDA", 5: "EP_ERR_NOT_READY"}

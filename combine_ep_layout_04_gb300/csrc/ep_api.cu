@@ -151,7 +151,7 @@ ep_status ep_config_check(const ep_config *c) {
     if (c->batch < 1 || c->batch > 8) return EP_ERR_INVALID_ARG;
     if (c->rows_per_msg < 0 || c->rows_per_msg > 2047) return EP_ERR_INVALID_ARG;   // 11 bits in a ring slot
     if (c->drain_batch < 32 || c->drain_batch > 512 || c->drain_batch % 32 != 0) return EP_ERR_INVALID_ARG;
-    if (c->debug_flags & ~EP_DEBUG_DISABLE_CONSUMER) return EP_ERR_INVALID_ARG;
+    if (c->debug_flags & ~(EP_DEBUG_DISABLE_CONSUMER | EP_DEBUG_DEVICE_COUNTERS)) return EP_ERR_INVALID_ARG;
     if (c->num_sms < 0 || (c->num_sms > 0 && c->num_sms < c->channels + 1) || c->reserved != 0)
         return EP_ERR_INVALID_ARG;
     const int64_t T = static_cast<int64_t>(c->num_ranks) * c->tokens_per_rank;

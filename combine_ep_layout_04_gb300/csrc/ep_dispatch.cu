@@ -128,19 +128,21 @@ struct SmemLayout {
     }
     static constexpr int kListBytesPerWarp = 32 * kListPerLane * 16;
     // message counters (G > 1): per (source, destination of the ring) the
-    // first counter of the pair's messages, then one counter per message; in
-    // the space below meta_off that copy CTAs give to stages
+    // first counter of the pair's messages, then one 16-bit counter per
+    // message; in the space below scratch_off that copy CTAs give to stages
+    // and meta slots, at least kCounterBytes of it
     __host__ __device__ static int counters_off(int R, int C, int D, int npw) {
         return (lists_off(R, C, D, npw) + npw * kListBytesPerWarp + 15) & ~15;
     }
+    static constexpr int kCounterBytes = 32768;
     // npw: the poster warps that run (fewer when their ranges would not fit
-    // beside the ring, e.g. 64 destinations on one channel)
-    __host__ __device__ SmemLayout(int R, int C, int D, int stage_bytes, int stages, int npw) {
+    // beside the ring, e.g. 64 destinations on one channel); G: rows per message
+    __host__ __device__ SmemLayout(int R, int C, int D, int stage_bytes, int stages, int npw, int G) {
         stage_off = 0;
         // channel CTAs keep the pair tables (3 x R x R ints) and their ring
         // (D slots of 16 bytes) where copy CTAs keep their stages
         const int stage_area = stage_bytes * stages,
-                  channel = lists_off(R, C, D, npw) + npw * kListBytesPerWarp;
+                  channel = counters_off(R, C, D, npw) + (G > 1 ? kCounterBytes : 0);
         meta_off = stage_area > channel ? stage_area : channel;
         meta_slot_bytes = ((32 * R + 33) + 3) / 4 * 16;   // dst[32*R] | pref[33]
         scratch_off = meta_off + meta_slot_bytes * kMetaSlots;
@@ -848,14 +850,120 @@ struct PairTables {
     const int *cnt, *recv0, *send0;
 };
 
+// The messages of pair (s, d) that one chunk's rows [jlo, jhi] of the pair
+// touch: g in [ga, gz], message g being rows [gG, min(gG + G, cnt)).  A
+// message that also has rows outside the chunk (G > 1) is shared with other
+// chunks and posted by whichever of them lands last: each adds the rows it
+// holds (rowsa, rowsz) to the message's counter, and the add that brings the
+// count to the message's size posts it.
+struct MsgSpan {
+    int ga, gz, za, zz, enda, endz;
+    unsigned rowsa, rowsz;
+    bool sha, shz;   // first / last message shared with other chunks
+    // lh: the chunk's first and last receive rows for the pair; false when
+    // they are not rows of the pair
+    __device__ __forceinline__ bool init(int2 lh, int cnt, int r0, int G) {
+        const int jlo = lh.x - r0, jhi = lh.y - r0;
+        if (jlo < 0 || jhi < jlo || jhi >= cnt) return false;
+        ga = jlo / G;
+        gz = jhi / G;
+        za = ga * G;
+        zz = gz * G;
+        enda = min(za + G, cnt) - 1;
+        endz = min(zz + G, cnt) - 1;
+        sha = G > 1 && (za < jlo || (ga == gz && enda > jhi));
+        shz = G > 1 && ga != gz && endz > jhi;
+        rowsa = static_cast<unsigned>(min(enda, jhi) - max(za, jlo) + 1);
+        rowsz = static_cast<unsigned>(jhi - zz + 1);
+        return true;
+    }
+    // messages [gb, ge) this chunk posts, given the counters' values before
+    // its adds; fa / fz: its add completed the first / last message
+    __device__ __forceinline__ int2 posts(unsigned olda, unsigned oldz, bool &fa, bool &fz) const {
+        int gb = ga, ge = gz + 1;
+        fa = sha && olda + rowsa == static_cast<unsigned>(enda - za + 1);
+        fz = shz && oldz + rowsz == static_cast<unsigned>(endz - zz + 1);
+        if (sha && !fa) {
+            if (ga == gz)
+                ge = gb;
+            else
+                gb = ga + 1;
+        }
+        if (shz && !fz) ge = gz;
+        return make_int2(gb, ge);
+    }
+};
+
+// Adds v to 16-bit counter m of a shared-memory array of them (two to a
+// word; a count never reaches 2^16) and returns its old value.
+__device__ __forceinline__ unsigned add_half_counter(unsigned *ctr, int m, unsigned v) {
+    const int sh = (m & 1) * 16;
+    return (atom_add_acq_rel_cta_shared(ctr + (m >> 1), v << sh) >> sh) & 0xffffu;
+}
+
+// The poster's span pass for counters in device memory (a ring whose
+// messages outnumber its shared-memory room): relaxed adds, kNoticeLoads
+// destinations' adds in flight at once, bracketed by a release fence before
+// them and an acquire fence after a completing one; a completed counter is
+// left at zero for the next call.  Writes the chunk's messages to post per
+// destination to rg[0, nd) and returns their number, or -1 when a notice
+// is out of range.
+__device__ __forceinline__ int device_counter_spans(unsigned *msg_rows, PairTables pt, int R, int C, int G, int c, int s,
+                                                 int nd, const int32_t *nt, int2 *rg) {
+    int total = 0;
+    bool bad = false;
+    fence_acq_rel_gpu();
+    bool done = false;
+    for (int i0 = 0; i0 < nd; i0 += kNoticeLoads) {
+        int2 lhs[kNoticeLoads];
+        unsigned olda[kNoticeLoads], oldz[kNoticeLoads];
+#pragma unroll
+        for (int b = 0; b < kNoticeLoads; ++b)
+            lhs[b] = i0 + b < nd ? __ldcg(reinterpret_cast<const int2 *>(nt + 2 * (c + (i0 + b) * C)))
+                                 : make_int2(-1, -1);
+#pragma unroll
+        for (int b = 0; b < kNoticeLoads; ++b) {
+            const int d = c + (i0 + b) * C;
+            MsgSpan sp;
+            olda[b] = oldz[b] = 0u;
+            if (lhs[b].y >= 0 && sp.init(lhs[b], pt.cnt[s * R + d], pt.recv0[s * R + d], G)) {
+                unsigned *q = msg_rows + pt.send0[s * R + d];
+                if (sp.sha) olda[b] = atom_add_relaxed(q + sp.za, sp.rowsa);
+                if (sp.shz) oldz[b] = atom_add_relaxed(q + sp.zz, sp.rowsz);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kNoticeLoads; ++b) {
+            const int i = i0 + b, d = c + i * C;
+            if (i >= nd) continue;
+            int2 r = make_int2(0, 0);
+            MsgSpan sp;
+            if (lhs[b].y >= 0 && !sp.init(lhs[b], pt.cnt[s * R + d], pt.recv0[s * R + d], G)) {
+                bad = true;
+            } else if (lhs[b].y >= 0) {
+                bool fa, fz;
+                r = sp.posts(olda[b], oldz[b], fa, fz);
+                unsigned *q = msg_rows + pt.send0[s * R + d];
+                if (fa) q[sp.za] = 0u;
+                if (fz) q[sp.zz] = 0u;
+                done = done || fa || fz;
+            }
+            rg[i] = r;
+            total += r.y - r.x;
+        }
+    }
+    if (done) fence_acq_rel_gpu();
+    return bad ? -1 : total;
+}
+
 // The posters of ring c.  Poster warp w takes chunk groups w, w + kPosterWarps,
 // ... of 32 chunks, lane i holding chunk 32 * group + i.  It polls the
 // group's ready flags and takes, pass by pass, the chunks found ready: each
 // such lane loads its chunk's notice for every destination of ring c (one
 // round trip) and derives the messages the chunk completes on ring c: those
-// of pair (s, d) whose last row lies in the chunk's rows [jlo, jhi] of the
-// pair -- all earlier rows of the pair are in earlier chunks.  The ranges go
-// to shared memory.  Then every lane writes its chunk's next commands (packed
+// of pair (s, d) all of whose rows lie in the chunk's rows [jlo, jhi] of the
+// pair, and those it shares with other chunks whose counter its add brings to
+// the message's size (MsgSpan).  The ranges go to shared memory.  Then every lane writes its chunk's next commands (packed
 // as a slot holds them) into the warp's list -- a walk along its own ranges,
 // no search -- and the warp posts the list one command per lane, 32 a round:
 // the first lane of each batch of up to `batch` lanes reserves the batch's
@@ -922,13 +1030,13 @@ __device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long
             pending = pending && !take_now;
             // this lane's chunk: messages [gb, ge) per destination of ring c
             int total = 0;
-            {
+            if (take_now) {
+                const int s = chunk_src(p, k);
+                const int32_t *nt = p.dev.notice + static_cast<int64_t>(k) * 2 * R;
                 bool bad = false;
-                if (take_now) {
-                    const int s = chunk_src(p, k);
-                    const int32_t *nt = p.dev.notice + static_cast<int64_t>(k) * 2 * R;
-                    // kNoticeLoads destinations' notices in flight at once
-                    int2 lhs[kNoticeLoads];
+                if (G == 1 || ctr_smem != nullptr) {
+                    // single-row messages, or counters in shared memory
+                    int2 lhs[kNoticeLoads];   // kNoticeLoads destinations' notices in flight at once
                     for (int i = 0; i < nd; ++i) {
                         const int d = c + i * C;
                         if (i % kNoticeLoads == 0) {
@@ -941,62 +1049,30 @@ __device__ void poster_warp(const DispatchParams &p, int c, int w, unsigned long
 #pragma unroll
                         for (int b = 1; b < kNoticeLoads; ++b)
                             if (i % kNoticeLoads == b) lh = lhs[b];
-                        int gb = 0, ge = 0;
-                        if (lh.y >= 0) {
-                            const int cnt = pt.cnt[s * R + d], r0 = pt.recv0[s * R + d];
-                            const int jlo = lh.x - r0, jhi = lh.y - r0;
-                            if (jlo < 0 || jhi < jlo || jhi >= cnt) {
-                                bad = true;
-                            } else {
-                                // messages g in [ga, gz] have rows here; message g
-                                // is rows [gG, min(gG + G, cnt)) of the pair
-                                const int ga = jlo / G, gz = jhi / G;
-                                gb = ga;
-                                ge = gz + 1;
-                                if (G > 1) {
-                                    // a message with rows outside this chunk is posted
-                                    // by whichever of its chunks lands last: each adds
-                                    // the rows it holds to the message's counter
-                                    const int za = ga * G, zz = gz * G;
-                                    const int enda = min(za + G, cnt) - 1, endz = min(zz + G, cnt) - 1;
-                                    // true when these rows complete message g (its counter
-                                    // is left at zero for the next call)
-                                    auto lands = [&](int g, int z, unsigned rows, int size) -> bool {
-                                        if (ctr_smem != nullptr) {
-                                            unsigned *q = ctr_smem + msgoff[s * nd + i] + g;
-                                            if (atom_add_acq_rel_cta_shared(q, rows) + rows != static_cast<unsigned>(size))
-                                                return false;
-                                            *q = 0u;
-                                        } else {
-                                            unsigned *q = p.msg_rows + pt.send0[s * R + d] + z;
-                                            if (atom_add_acq_rel(q, rows) + rows != static_cast<unsigned>(size)) return false;
-                                            *q = 0u;
-                                        }
-                                        return true;
-                                    };
-                                    if (ga == gz) {
-                                        if ((za < jlo || enda > jhi) &&
-                                            !lands(ga, za, static_cast<unsigned>(jhi - jlo + 1), enda - za + 1))
-                                            ge = gb;
-                                    } else {
-                                        if (za < jlo && !lands(ga, za, static_cast<unsigned>(enda - jlo + 1), enda - za + 1))
-                                            gb = ga + 1;
-                                        if (endz > jhi && !lands(gz, zz, static_cast<unsigned>(jhi - zz + 1), endz - zz + 1))
-                                            ge = gz;
-                                    }
-                                }
-                            }
+                        int2 r = make_int2(0, 0);
+                        MsgSpan sp;
+                        if (lh.y >= 0 && !sp.init(lh, pt.cnt[s * R + d], pt.recv0[s * R + d], G)) {
+                            bad = true;
+                        } else if (lh.y >= 0) {
+                            const int m0 = sp.sha || sp.shz ? msgoff[s * nd + i] : 0;
+                            const unsigned olda = sp.sha ? add_half_counter(ctr_smem, m0 + sp.ga, sp.rowsa) : 0u;
+                            const unsigned oldz = sp.shz ? add_half_counter(ctr_smem, m0 + sp.gz, sp.rowsz) : 0u;
+                            bool fa, fz;
+                            r = sp.posts(olda, oldz, fa, fz);
                         }
-                        ranges[lane * ndmax + i] = make_int2(gb, ge);
-                        total += ge - gb;
+                        ranges[lane * ndmax + i] = r;
+                        total += r.y - r.x;
                     }
+                } else {
+                    total = device_counter_spans(p.msg_rows, pt, R, C, G, c, s, nd, nt, ranges + lane * ndmax);
+                    bad = total < 0;
                 }
                 if (bad) {
                     set_error(p.dev.err, EP_ERR_INVALID_ARG);
                     total = 0;
                 }
-                __syncwarp();
             }
+            __syncwarp();
             // Post the group's commands.  Each lane lists its own chunk's next
             // commands (at most kListPerLane) into the warp's list, packed the way
             // a slot holds them; the warp then posts the list, 32 (whole batches)
@@ -1261,7 +1337,7 @@ __device__ void consumer_log(const DispatchParams &p, int c, long long expected,
 
 __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    const SmemLayout L(p.R, p.C, p.D, p.stage_bytes, p.stages, p.poster_warps);
+    const SmemLayout L(p.R, p.C, p.D, p.stage_bytes, p.stages, p.poster_warps, p.G);
     int *rbase = reinterpret_cast<int *>(smem + L.scratch_off);
     unsigned long long *words =
         reinterpret_cast<unsigned long long *>(smem + L.scratch_off + ((p.R + 3) & ~3) * 4);
@@ -1358,12 +1434,14 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
     __syncthreads();
     if (channel_cta && p.G > 1) {
         // message counters of this ring: the first one of each
-        // pair (s, d), d = c + i*C, in (s, i) order, then one per message, in
-        // shared memory if they fit; else the device-memory counters are used
+        // pair (s, d), d = c + i*C, in (s, i) order, then one 16-bit counter
+        // per message, in shared memory if they fit; else the device-memory
+        // counters are used
         const int c = blockIdx.x;
         const int nd = c < p.R ? (p.R - 1 - c) / p.C + 1 : 0;
         const int coff = SmemLayout::counters_off(p.R, p.C, p.D, p.poster_warps);
-        const long long room = static_cast<long long>(L.meta_off - coff) / 4 - static_cast<long long>(p.R) * nd;
+        // counters are 16-bit halves of a word
+        const long long room = 2 * (static_cast<long long>(L.scratch_off - coff) / 4 - static_cast<long long>(p.R) * nd);
         if (warp == 1) {
             int *msgoff = reinterpret_cast<int *>(smem + coff);
             const int *cntt = reinterpret_cast<const int *>(smem);
@@ -1385,12 +1463,14 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
                 run += __shfl_sync(kFull, incl, 31);
             }
             if (lane == 0)
-                words[kWCounters] = room >= 0 && run <= room ? static_cast<unsigned long long>(run) + 1ull : 0ull;
+                words[kWCounters] = !(p.debug & EP_DEBUG_DEVICE_COUNTERS) && room >= 0 && run <= room
+                                        ? static_cast<unsigned long long>(run) + 1ull
+                                        : 0ull;
         }
         __syncthreads();
         if (words[kWCounters] != 0ull) {
             unsigned *ctr = reinterpret_cast<unsigned *>(smem + coff) + p.R * nd;
-            const int n = static_cast<int>(words[kWCounters] - 1ull);
+            const int n = static_cast<int>((words[kWCounters] - 1ull + 1ull) / 2);   // words of two counters
             for (int i = threadIdx.x; i < n; i += blockDim.x) ctr[i] = 0u;
             __syncthreads();
         }
@@ -1484,7 +1564,7 @@ ep_status plan_dispatch(ep_ctx *h) {
     int stages = 0, npw = kPosterWarpsMax;
     for (; npw >= 1 && stages == 0; npw /= 2) {
         for (int s = kStagesMax; s >= 3; --s) {
-            SmemLayout L(R, C, h->cfg.ring_depth, stage_bytes, s, npw);
+            SmemLayout L(R, C, h->cfg.ring_depth, stage_bytes, s, npw, static_cast<int>(h->G));
             if (L.total + reserve <= max_smem) {
                 stages = s;
                 break;
@@ -1493,7 +1573,7 @@ ep_status plan_dispatch(ep_ctx *h) {
         if (stages) break;
     }
     if (stages == 0) return EP_ERR_INVALID_ARG;
-    SmemLayout L(R, C, h->cfg.ring_depth, stage_bytes, stages, npw);
+    SmemLayout L(R, C, h->cfg.ring_depth, stage_bytes, stages, npw, static_cast<int>(h->G));
     h->poster_warps = npw;
     h->rows_per_item = rows_per_item;
     h->vec_store = (pieces == 1 && B <= kVecRowMax) ? 1 : 0;

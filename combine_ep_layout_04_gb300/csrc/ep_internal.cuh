@@ -214,6 +214,12 @@ __device__ __forceinline__ unsigned int atom_add_acq_rel(unsigned int *p, unsign
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
 }
+// relaxed atomic add (GPU scope); returns the old value
+__device__ __forceinline__ unsigned int atom_add_relaxed(unsigned int *p, unsigned int v) {
+    unsigned int old;
+    asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
 __device__ __forceinline__ unsigned int atom_add_acq_rel_cta_shared(unsigned int *p, unsigned int v) {
     unsigned int old;
     asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"

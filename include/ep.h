@@ -90,6 +90,11 @@ typedef struct {
 /* Test hook: ring consumers do not run, so producers see a full ring and their
  * bounded flow-control wait ends in EP_ERR_TIMEOUT (no GPU hang, no trap). */
 #define EP_DEBUG_DISABLE_CONSUMER 0x1
+/* Test hook: the per-message landed-row counters of multi-row messages
+ * (rows_per_msg > 1) live in device memory even where a ring's counters fit in
+ * its shared memory -- the path taken when a ring's messages outnumber that
+ * room.  Results are unchanged. */
+#define EP_DEBUG_DEVICE_COUNTERS 0x2
 
 /* One ring record ([UCCL-EP] s2.3 TransferCmd; WRITE only), 32 bytes.
  *  dst_rank:   destination rank d.

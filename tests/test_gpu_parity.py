@@ -112,20 +112,52 @@ def _w(**kw):
     dict(num_ranks=64, tokens_per_rank=24, hidden=2048, num_experts=256, topk=8),  # 4 KB rows, 64 ranks
     dict(num_ranks=16, tokens_per_rank=1, hidden=1024, num_experts=32, topk=4),    # one token per rank
     dict(num_ranks=8, tokens_per_rank=97, hidden=2056, num_experts=32, topk=6),    # 4112-byte rows: TMA path
+    dict(num_ranks=6, tokens_per_rank=40, hidden=14336, num_experts=12, topk=3),   # 28 KB rows: 2 pieces
+    dict(num_ranks=4, tokens_per_rank=24, hidden=28672, num_experts=8, topk=2),    # 56 KB rows: 4 pieces
+    dict(num_ranks=2, tokens_per_rank=12, hidden=524288, num_experts=2, topk=2),   # 1 MB rows: 64 pieces
 ])
 def test_edge_shapes(kw):
     run_and_check(_w(**kw))
+
+
+def test_one_16mb_message():
+    # one rank, 2047 rows of 8 KB in one message (the most a message holds):
+    # a 16 MB TransferCmd
+    w = _w(num_ranks=1, tokens_per_rank=2047, hidden=4096, num_experts=1, topk=1)
+    layer, lay_o = run_and_check(w, rows_per_msg=2047)
+    ref, per = oracle.descriptors(lay_o, 8, 2047, 2 * 4096)
+    assert len(ref) == 1 and int(ref["size"][0]) == 2047 * 8192
 
 
 @pytest.mark.parametrize("opts", [
     dict(rows_per_msg=1), dict(rows_per_msg=3), dict(rows_per_msg=64), dict(batch=1), dict(channels=1),
     dict(channels=3), dict(ring_depth=16, max_inflight=8), dict(ring_depth=64, max_inflight=64, batch=5),
     dict(drain_batch=64), dict(ring_depth=8192, max_inflight=8192), dict(rows_per_msg=2047),
-    dict(drain_batch=512, max_inflight=512),
+    dict(drain_batch=512, max_inflight=512), dict(rows_per_msg=3, debug_flags=2),
+    dict(rows_per_msg=64, debug_flags=2), dict(rows_per_msg=5, channels=1, debug_flags=2),
 ])
 def test_ring_options(opts):
     w = _w(num_ranks=8, tokens_per_rank=100, hidden=512, num_experts=32, topk=4)
     run_and_check(w, **opts)
+
+
+@pytest.mark.parametrize("dev_counters", [False, True])
+def test_multi_row_messages_twice(dev_counters):
+    # messages of 4 rows spanning chunks, posted by whichever chunk lands last;
+    # a second call on the same handle finds every counter back at zero
+    from combine_ep_layout_04_gb300 import _ep
+    w = W.get("small")
+    idx, wt, x = workload_inputs(w)
+    with make_layer(w, rows_per_msg=4, debug_flags=_ep.EP_DEBUG_DEVICE_COUNTERS if dev_counters else 0) as layer:
+        topk = torch.from_numpy(idx).cuda()
+        lay_o = oracle.layout(w.num_ranks, w.tokens_per_rank, w.num_experts, idx, 4)
+        for _ in range(2):
+            lay = layer.layout(topk)
+            recv = layer.dispatch(x, lay)
+            torch.cuda.synchronize()
+            assert layer.device_status() == 0
+            check_dispatch_rows(recv, x, lay_o)
+            compare_descriptors(layer.cmd_log(), lay_o, layer.cfg.channels, 4, 2 * w.hidden)
 
 
 def test_many_destinations_per_channel():
