@@ -9,7 +9,7 @@ intervals on the launching stream.  Prints one JSON line.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload ht]
   python bench.py --impl reference ...   # the CPU oracle on the host, same metric
   python bench.py --sweep msg            # dispatch bandwidth against row and message size
-  python bench.py --overlap              # layer pieces: sequential against pipelined
+  python bench.py --overlap              # communication/computation overlap experiments
   python bench.py --tokens-per-rank 256  # a smaller case of a workload (profiler captures)
 
 Beside the step, the JSON line carries `next_rows.expert_layout`: ep_expert_layout
@@ -317,8 +317,9 @@ def main():
     ap.add_argument("--tokens-per-rank", type=int, default=0,
                     help="override the workload's tokens per rank (smaller cases for profiler captures)")
     ap.add_argument("--overlap", action="store_true",
-                    help="time dispatch -> stand-in expert GEMM -> combine over source-rank pieces, "
-                         "sequential against pipelined on three streams")
+                    help="two micro-batches of dispatch -> stand-in expert GEMM -> combine, sequential "
+                         "against overlapped on communication and compute streams (with and without disjoint "
+                         "SM partitions), and the expert layout beside the dispatch")
     ap.add_argument("--sweep", choices=["msg"], default=None,
                     help="msg: dispatch bandwidth against row and message size, one JSON line per point")
     ap.add_argument("--points", default=None,
@@ -573,22 +574,27 @@ def time_expert_layout(case, peak, reps: int = 20):
 
 
 # ------------------------------------------------------------------- overlap
-def run_overlap(args, w, pieces: int = 4, gemm_cols: int = 256, reps: int = 10):
-    """Dispatch -> expert work -> combine of one layer, split into `pieces`
-    pieces of consecutive source ranks (ep_dispatch_ranks / ep_combine_tokens).
-    The expert work is a stand-in: one bf16 GEMM per piece, [N/pieces, H] x
-    [H, gemm_cols] with cuBLAS (torch.matmul), ordered after the piece's
-    dispatch and before its combine; combine reads the receive buffer
-    (identity expert), so the GEMM only occupies the GPU the way expert work
-    would.  Sequential: everything on one stream with every SM.  Pipelined:
-    dispatch pieces back to back on one stream, each piece's GEMM on a second
-    stream once the piece has landed, each piece's combine on a third once
-    its GEMM is done, with dispatch and combine limited to `num_sms` SMs.
-    One JSON line per SM budget."""
+def run_overlap(args, w, gemm_cols: int = 2048, reps: int = 8):
+    """Overlap of the layer's data movement with computation, two experiments.
+
+    1. Two micro-batches (two independent layers of this workload's shape,
+       each with its own handle), each dispatch -> expert -> combine.  The
+       expert is a stand-in: y = recv @ W, a bf16 cuBLAS GEMM [N, H] x
+       [H, gemm_cols] (2048 is DeepSeek-V3's expert intermediate size); the
+       combine reads recv (identity expert).  Sequential: everything on one
+       stream with every SM.  Overlapped: dispatch A, dispatch B, combine A,
+       combine B on a communication stream; expert A after dispatch A and
+       expert B after dispatch B on a compute stream; combine X after expert
+       X -- ordered by events only.  Either on disjoint SM partitions
+       (SmSplit: the compute stream gets `compute_sms`, the handle num_sms =
+       the rest) or unpartitioned (two ordinary streams, communication at the
+       higher priority).  Outputs must equal the sequential ones.
+    2. Our own latency-bound consumer beside the dispatch (below).
+    One JSON line per configuration."""
     import torch
 
     import workloads as W
-    from combine_ep_layout_04_gb300 import EpLayer
+    from combine_ep_layout_04_gb300 import EpLayer, SmSplit
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
@@ -599,10 +605,6 @@ def run_overlap(args, w, pieces: int = 4, gemm_cols: int = 256, reps: int = 10):
     topk = torch.from_numpy(idx).to(dev)
     wts = torch.from_numpy(wt).to(dev)
     x = W.make_x_torch(w, dev)
-    g = torch.Generator(device=dev)
-    g.manual_seed(w.seed + 17)
-    Wg = (torch.randn((H, gemm_cols), device=dev, generator=g) * 0.02).to(torch.bfloat16)
-    bounds = [(i * R // pieces, (i + 1) * R // pieces) for i in range(pieces)]
 
     def timed(fn, streams):
         ts = []
@@ -633,70 +635,113 @@ def run_overlap(args, w, pieces: int = 4, gemm_cols: int = 256, reps: int = 10):
         out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
         return L, lay, recv, out
 
-    L, lay, recv, out = make(0)
-    N = lay.n_recv
-    rows = [(i * N // pieces, (i + 1) * N // pieces) for i in range(pieces)]
-    ys = [torch.empty((b - a, gemm_cols), dtype=torch.bfloat16, device=dev) for a, b in rows]
+    # ---- 1. two micro-batches
+    mbs = []
+    for m in range(2):
+        wm = W.Workload(f"{w.name}-mb{m}", R, Tpr, H, w.num_experts, w.topk, routing=w.routing, zipf_s=w.zipf_s,
+                        seed=w.seed + 1000 * m)
+        i_m, wt_m = W.make_routing(wm)
+        mbs.append(dict(topk=torch.from_numpy(i_m).to(dev), wts=torch.from_numpy(wt_m).to(dev),
+                        x=W.make_x_torch(wm, dev)))
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed + 17)
+    Wg = (torch.randn((H, gemm_cols), device=dev, generator=g) * 0.02).to(torch.bfloat16)
 
-    def gemm(i):
-        torch.matmul(recv[rows[i][0]:rows[i][1]], Wg, out=ys[i])
+    def layers(num_sms):
+        cs = []
+        for mb in mbs:
+            L = EpLayer(R, Tpr, H, w.num_experts, w.topk, channels=w.channels, ring_depth=w.ring_depth,
+                        max_inflight=w.max_inflight, rows_per_msg=w.rows_per_msg, num_sms=num_sms, device=dev)
+            lay = L.layout(mb["topk"])
+            cs.append(dict(L=L, lay=lay, recv=torch.empty((lay.n_recv, H), dtype=torch.bfloat16, device=dev),
+                           out=torch.empty((T, H), dtype=torch.bfloat16, device=dev),
+                           y=torch.empty((lay.n_recv, gemm_cols), dtype=torch.bfloat16, device=dev), **mb))
+        return cs
 
-    def comm_only():
-        for a, b in bounds:
-            L.dispatch(x, lay, recv, src_ranks=(a, b))
-        for a, b in bounds:
-            L.combine(recv, wts, topk, lay, out=out, tokens=(a * Tpr, b * Tpr))
+    def disp(c):
+        c["L"].dispatch(c["x"], c["lay"], c["recv"])
 
-    def gemm_only():
-        for i in range(pieces):
-            gemm(i)
+    def comb(c):
+        c["L"].combine(c["recv"], c["wts"], c["topk"], c["lay"], out=c["out"])
+
+    def expert(c):
+        torch.matmul(c["recv"], Wg, out=c["y"])
+
+    cs = layers(0)
 
     def sequential():
-        for a, b in bounds:
-            L.dispatch(x, lay, recv, src_ranks=(a, b))
-        gemm_only()
-        for a, b in bounds:
-            L.combine(recv, wts, topk, lay, out=out, tokens=(a * Tpr, b * Tpr))
+        for c in cs:
+            disp(c)
+            expert(c)
+            comb(c)
 
-    t_comm = timed(comm_only, [])
-    t_gemm = timed(gemm_only, [])
     t_seq = timed(sequential, [])
-    if L.device_status() != 0:
-        raise SystemExit(f"device status {L.device_status()} in the overlap run")
-    L.close()
-    flops = 2.0 * N * H * gemm_cols
-    for budget in (0, 120, 96, 64):
-        Lb, layb, recvb, outb = make(budget)
-        sG, sC = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    t_comm = timed(lambda: [f(c) for c in cs for f in (disp, comb)], [])
+    t_exp = timed(lambda: [expert(c) for c in cs], [])
+    ref = [c["out"].clone() for c in cs]
+    n_recv = [int(c["lay"].n_recv) for c in cs]
+    for c in cs:
+        c["L"].close()
+    flops = 2.0 * sum(n_recv) * H * gemm_cols
+    base = {"overlap": w.name, "experiment": "two micro-batches", "gemm_cols": gemm_cols,
+            "stand_in": f"bf16 cuBLAS GEMM [N, {H}] x [{H}, {gemm_cols}] per micro-batch",
+            "sequential_ms": round(t_seq, 3), "comm_alone_ms": round(t_comm, 3), "expert_alone_ms": round(t_exp, 3),
+            "expert_tflops": round(flops / t_exp / 1e9, 1)}
+    for compute_sms in (None, 48, 72, 96):
+        sp = SmSplit(compute_sms, device=dev) if compute_sms else None
+        cs = layers(sp.comm_sms if sp else 0)
+        sc = sp.comm if sp else torch.cuda.Stream(dev, priority=-1)
+        sg = sp.compute if sp else torch.cuda.Stream(dev, priority=0)
 
-        def pipelined():
-            main = torch.cuda.current_stream(dev)
-            for i, (a, b) in enumerate(bounds):
-                Lb.dispatch(x, layb, recvb, src_ranks=(a, b))
-                ev = torch.cuda.Event()
-                ev.record(main)
-                sG.wait_event(ev)
-                with torch.cuda.stream(sG):
-                    torch.matmul(recvb[rows[i][0]:rows[i][1]], Wg, out=ys[i])
-                    eg = torch.cuda.Event()
-                    eg.record(sG)
-                sC.wait_event(eg)
-                with torch.cuda.stream(sC):
-                    Lb.combine(recvb, wts, topk, layb, out=outb, tokens=(a * Tpr, b * Tpr))
+        def overlapped():
+            ev_d, ev_g = [], []
+            with torch.cuda.stream(sc):
+                for c in cs:
+                    disp(c)
+                    ev_d.append(torch.cuda.Event())
+                    ev_d[-1].record(sc)
+            with torch.cuda.stream(sg):
+                for c, e in zip(cs, ev_d):
+                    sg.wait_event(e)
+                    expert(c)
+                    ev_g.append(torch.cuda.Event())
+                    ev_g[-1].record(sg)
+            with torch.cuda.stream(sc):
+                for c, e in zip(cs, ev_g):
+                    sc.wait_event(e)
+                    comb(c)
 
-        t_pipe = timed(pipelined, [sG, sC])
-        if Lb.device_status() != 0:
-            raise SystemExit(f"device status {Lb.device_status()} in the pipelined run")
-        if not torch.equal(outb.view(torch.int16), out.view(torch.int16)):
-            raise SystemExit("pipelined output differs from the sequential one")
-        Lb.close()
-        row = {"overlap": w.name, "pieces": pieces, "num_sms": budget or props.multi_processor_count,
-               "comm_ms": round(t_comm, 3), "gemm_ms": round(t_gemm, 3),
-               "gemm_tflops": round(flops / t_gemm / 1e9, 1), "sequential_ms": round(t_seq, 3),
-               "pipelined_ms": round(t_pipe, 3), "speedup": round(t_seq / t_pipe, 3),
-               "hidden_fraction": round((t_seq - t_pipe) / min(t_comm, t_gemm), 3),
-               "stand_in": f"bf16 GEMM [N/{pieces}, {H}] x [{H}, {gemm_cols}] per piece (cuBLAS)"}
+        def comm_part():
+            with torch.cuda.stream(sc):
+                for c in cs:
+                    disp(c)
+                for c in cs:
+                    comb(c)
+
+        def expert_part():
+            with torch.cuda.stream(sg):
+                for c in cs:
+                    expert(c)
+
+        t_ovl = timed(overlapped, [sc, sg])
+        if any(c["L"].device_status() != 0 for c in cs):
+            raise SystemExit("device status set in the overlapped run")
+        if not all(torch.equal(c["out"].view(torch.int16), r.view(torch.int16)) for c, r in zip(cs, ref)):
+            raise SystemExit("overlapped output differs from the sequential one")
+        row = dict(base, partition=("disjoint SMs (green contexts)" if sp else "none (stream priorities)"),
+                   comm_sms=sp.comm_sms if sp else props.multi_processor_count,
+                   compute_sms=sp.compute_sms if sp else props.multi_processor_count,
+                   overlapped_ms=round(t_ovl, 3), speedup=round(t_seq / t_ovl, 3))
+        if sp:
+            row["comm_on_partition_ms"] = round(timed(comm_part, [sc]), 3)
+            row["expert_on_partition_ms"] = round(timed(expert_part, [sg]), 3)
         print(json.dumps(row), flush=True)
+        for c in cs:
+            c["L"].close()
+        del cs
+        if sp:
+            sp.close()
+        torch.cuda.empty_cache()
 
     # Our own consumer beside the dispatch: ep_expert_layout needs only the
     # layout, is latency-bound, and can use SMs the dispatch leaves free.

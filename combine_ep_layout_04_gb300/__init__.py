@@ -10,11 +10,11 @@ there is no fallback path.  (The exports load lazily so that build.py can be
 imported before the library exists.)
 """
 
-__all__ = ["EpLayer", "Layout", "ExpertLayout", "EpError", "CMD_DTYPE"]
+__all__ = ["EpLayer", "Layout", "ExpertLayout", "SmSplit", "EpError", "CMD_DTYPE"]
 
 
 def __getattr__(name):
-    if name in ("EpLayer", "Layout", "ExpertLayout", "CMD_DTYPE"):
+    if name in ("EpLayer", "Layout", "ExpertLayout", "SmSplit", "CMD_DTYPE"):
         from . import layer
         return getattr(layer, name)
     if name == "EpError":

@@ -105,6 +105,11 @@ _sigs = {
     "ep_get_info": ([_h, ctypes.POINTER(ep_info)], ctypes.c_int),
     "ep_layout_static": ([ctypes.POINTER(ep_config), _p, ctypes.POINTER(ep_layout_out),
                           ctypes.POINTER(ctypes.c_int64), _p], ctypes.c_int),
+    "ep_sm_split_create": ([ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(_h)], ctypes.c_int),
+    "ep_sm_split_get": ([_h, ctypes.POINTER(_p), ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(_p),
+                         ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
+    "ep_sm_split_destroy": ([_h], ctypes.c_int),
+    "ep_sm_ids": ([_p, ctypes.c_int32, _p], ctypes.c_int),
 }
 for _name, (_args, _res) in _sigs.items():
     _f = getattr(lib, _name)
@@ -245,3 +250,26 @@ def ep_get_info(h) -> dict:
     info = ep_info()
     check(lib.ep_get_info(h, ctypes.byref(info)), "ep_get_info")
     return {f: getattr(info, f) for f, _ in ep_info._fields_}
+
+
+def ep_sm_split_create(device: int, compute_sms: int):
+    s = ctypes.c_void_p()
+    check(lib.ep_sm_split_create(device, compute_sms, ctypes.byref(s)), "ep_sm_split_create")
+    return s
+
+
+def ep_sm_split_get(s) -> tuple:
+    """(comm_stream, comm_sms, compute_stream, compute_sms)"""
+    cs, ks = ctypes.c_void_p(), ctypes.c_void_p()
+    cn, kn = ctypes.c_int32(), ctypes.c_int32()
+    check(lib.ep_sm_split_get(s, ctypes.byref(cs), ctypes.byref(cn), ctypes.byref(ks), ctypes.byref(kn)),
+          "ep_sm_split_get")
+    return int(cs.value), int(cn.value), int(ks.value), int(kn.value)
+
+
+def ep_sm_split_destroy(s) -> None:
+    check(lib.ep_sm_split_destroy(s), "ep_sm_split_destroy")
+
+
+def ep_sm_ids(stream: int, blocks: int, out_ptr: int) -> None:
+    check(lib.ep_sm_ids(stream, blocks, out_ptr), "ep_sm_ids")

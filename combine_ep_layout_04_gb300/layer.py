@@ -290,3 +290,41 @@ class EpLayer:
 
     def reset(self) -> None:
         _ep.ep_reset(self.handle)
+
+
+class SmSplit:
+    """Two disjoint SM partitions of one GPU (ep_sm_split_create): `comm`, a
+    torch stream for layout/dispatch/combine (use an EpLayer made with
+    num_sms=comm_sms), and `compute`, a torch stream for the caller's
+    computation.  Order work between them with events only."""
+
+    def __init__(self, compute_sms: int, device=None):
+        self.device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        self._s = _ep.ep_sm_split_create(self.device.index, int(compute_sms))
+        cs, self.comm_sms, ks, self.compute_sms = _ep.ep_sm_split_get(self._s)
+        self.comm = torch.cuda.ExternalStream(cs, device=self.device)
+        self.compute = torch.cuda.ExternalStream(ks, device=self.device)
+
+    def sm_ids(self, stream, blocks: int = 4096) -> set:
+        """SM ids that `blocks` short blocks enqueued on `stream` ran on."""
+        out = torch.full((blocks,), -1, dtype=torch.int32, device=self.device)
+        _ep.ep_sm_ids(stream.cuda_stream, blocks, out.data_ptr())
+        stream.synchronize()
+        return set(out.cpu().tolist())
+
+    def close(self) -> None:
+        if self._s is not None:
+            _ep.ep_sm_split_destroy(self._s)
+            self._s = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -406,6 +406,37 @@ ep_status ep_get_info(ep_handle h, ep_info *out);
 ep_status ep_layout_static(const ep_config *cfg, const int32_t *topk_idx, const ep_layout_out *out,
                            int64_t *n_recv_host, void *stream);
 
+/* SM partitions for overlapping the layer's data movement with computation
+ * (GPU communication notes, communication/computation overlap: DeepEP gives
+ * its dispatch and combine kernels a fixed SM budget and the rest of the GPU
+ * to the expert GEMMs).  ep_sm_split_create divides device `device`'s SMs into
+ * two disjoint partitions with the driver's green contexts: at least
+ * compute_sms SMs (rounded up to the device's partition granularity, 8 SMs
+ * on this architecture) for computation and the remainder for communication,
+ * each with a non-blocking stream whose work runs only on its partition.  The
+ * streams belong to the device's primary context, so device memory, events
+ * and every other stream work with them as usual.  To overlap, run
+ * ep_layout/ep_dispatch/ep_combine on the communication stream of a handle
+ * made with num_sms = the communication partition's SM count (a cooperative
+ * dispatch must fit in its partition), the caller's compute on the compute
+ * stream, and order the two with events only: no kernel on one stream may
+ * wait on the other's progress (partitions do not guarantee that both run at
+ * once).  compute_sms must leave SMs for communication, else
+ * EP_ERR_INVALID_ARG; driver failures are EP_ERR_CUDA.  The caller owns the
+ * split and frees it with ep_sm_split_destroy after the work queued on its
+ * streams (destroy waits for both streams first). */
+typedef struct ep_sm_split_s *ep_sm_split;
+ep_status ep_sm_split_create(int32_t device, int32_t compute_sms, ep_sm_split *out);
+/* The partitions' streams (cudaStream_t) and SM counts; any output may be NULL. */
+ep_status ep_sm_split_get(ep_sm_split split, void **comm_stream, int32_t *comm_sms, void **compute_stream,
+                          int32_t *compute_sms);
+ep_status ep_sm_split_destroy(ep_sm_split split);
+/* Diagnostic: enqueue on `stream` `blocks` (1..2^20) one-warp blocks that each
+ * run about 2 us and write the id of the SM they ran on to sm_ids_out[block]
+ * (caller-owned device int32 array).  Shows which SMs a stream's work may
+ * use. */
+ep_status ep_sm_ids(void *stream, int32_t blocks, int32_t *sm_ids_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -96,6 +96,18 @@ def test_null_handles_are_rejected(ep):
     assert ep.lib.ep_signal_get(None, None, 0) == ep.EP_ERR_INVALID_ARG
     assert ep.lib.ep_signal_reset(None, None) == ep.EP_ERR_INVALID_ARG
     assert ep.lib.ep_wait_signal(None, 0, 0, 0, None, None) == ep.EP_ERR_INVALID_ARG
+    assert ep.lib.ep_sm_split_get(None, None, None, None, None) == ep.EP_ERR_INVALID_ARG
+    assert ep.lib.ep_sm_split_destroy(None) == ep.EP_ERR_INVALID_ARG
+    assert ep.lib.ep_sm_ids(None, 1, None) == ep.EP_ERR_INVALID_ARG
+
+
+def test_sm_split_arguments_are_checked_before_the_device(ep):
+    import ctypes
+    s = ctypes.c_void_p()
+    assert ep.lib.ep_sm_split_create(0, 0, ctypes.byref(s)) == ep.EP_ERR_INVALID_ARG
+    assert ep.lib.ep_sm_split_create(-1, 8, ctypes.byref(s)) == ep.EP_ERR_INVALID_ARG
+    assert ep.lib.ep_sm_split_create(0, 8, None) == ep.EP_ERR_INVALID_ARG
+    assert ep.lib.ep_sm_ids(None, 0, None) == ep.EP_ERR_INVALID_ARG
 
 
 def test_struct_sizes_match_the_header(ep):

@@ -9,8 +9,8 @@ import torch
 
 import oracle
 import workloads as W
-from _helpers import (bf16_tensor_to_bits, bf16_ulp_distance, check_dispatch_rows, compare_descriptors,
-                      compare_layout, oracle_combine_sample, workload_inputs)
+from _helpers import (bf16_tensor_to_bits, bf16_ulp_distance, check_combine_all, check_dispatch_rows,
+                      compare_descriptors, compare_layout, oracle_combine_sample, workload_inputs)
 
 pytestmark = pytest.mark.gpu
 
@@ -176,3 +176,69 @@ def test_dispatch_plan_follows_the_grid(name, num_sms):
             assert info["dispatch_chunk_tokens"] == 32
     finally:
         layer.close()
+
+
+@pytest.mark.parametrize("compute_sms", [8, 64, 120])
+def test_sm_split_partitions_are_disjoint(compute_sms):
+    from combine_ep_layout_04_gb300 import SmSplit
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    with SmSplit(compute_sms) as sp:
+        assert sp.compute_sms >= compute_sms and sp.comm_sms >= 1
+        assert sp.comm_sms + sp.compute_sms <= n_sm
+        a, b = sp.sm_ids(sp.comm), sp.sm_ids(sp.compute)
+        assert not (a & b), "the partitions share SMs"
+        assert len(a) <= sp.comm_sms and len(b) <= sp.compute_sms
+        # 4096 blocks of 2 us reach every SM of a partition
+        assert len(a) == sp.comm_sms and len(b) == sp.compute_sms
+        everywhere = sp.sm_ids(torch.cuda.current_stream())
+        assert len(everywhere) == n_sm
+
+
+def test_sm_split_rejects_a_split_without_comm_sms():
+    from combine_ep_layout_04_gb300 import SmSplit, _ep
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    for bad in (0, n_sm, n_sm + 8):
+        with pytest.raises(_ep.EpError):
+            SmSplit(bad)
+
+
+@pytest.mark.parametrize("name", ["small", "ll"])
+def test_layer_on_the_comm_partition_beside_a_gemm(name):
+    # layout, dispatch and combine on the communication partition (grid =
+    # its SM count) while a GEMM loop runs on the compute partition: the
+    # results are the oracle's, and the GEMM's those of the same GEMM on the
+    # whole GPU
+    from combine_ep_layout_04_gb300 import SmSplit
+    w = W.get(name)
+    idx, wt, x = workload_inputs(w, x_on_device=True)
+    A = torch.randn((8192, 4096), device="cuda").to(torch.bfloat16)
+    B = (torch.randn((4096, 1024), device="cuda") * 0.02).to(torch.bfloat16)
+    ref_y = A @ B
+    with SmSplit(64) as sp:
+        layer = make_layer(w, num_sms=sp.comm_sms)
+        try:
+            assert layer.info["dispatch_grid"] == sp.comm_sms
+            topk = torch.from_numpy(idx).cuda()
+            wts = torch.from_numpy(wt).cuda()
+            torch.cuda.synchronize()
+            ys = []
+            with torch.cuda.stream(sp.compute):
+                for _ in range(20):
+                    ys.append(A @ B)
+            with torch.cuda.stream(sp.comm):
+                lay = layer.layout(topk)
+                recv = layer.dispatch(x, lay)
+                out = layer.combine(recv, wts, topk, lay)
+            torch.cuda.synchronize()
+            assert layer.device_status() == 0
+            lay_o = oracle.layout(w.num_ranks, w.tokens_per_rank, w.num_experts, idx, layer.G)
+            compare_layout(lay.numpy(), lay_o)
+            check_dispatch_rows(recv, x, lay_o)
+            compare_descriptors(layer.cmd_log(), lay_o, layer.cfg.channels, layer.G, 2 * w.hidden)
+            worst = check_combine_all(out, lay_o, idx, wt, w.experts_per_rank, recv, max_ulp=1)
+            assert worst <= 1
+            for y in ys:
+                assert torch.allclose(y.float(), ref_y.float(), rtol=1e-2, atol=1e-2)
+        finally:
+            layer.close()
+
