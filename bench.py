@@ -504,16 +504,20 @@ class GpuCase:
         if self.layer.device_status() != 0:
             raise SystemExit(f"device status {self.layer.device_status()} after warm-up ({self.w.name})")
 
-    def timed_steps(self, n, gate_s: float = 0.0):
+    def timed_steps(self, n, gate_s: float = 0.05):
         """Seconds of layout, dispatch and combine in each of n steps (CUDA
-        events on the launching stream)."""
+        events on the launching stream).  The stream is held for gate_s
+        while the host enqueues (outside the events), and Python's garbage
+        collector is off, so that the host runs ahead of the GPU and no op
+        between two events waits for its launch."""
+        import gc
+
         import torch
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
         torch.cuda.synchronize(self.dev)
+        gc_was = gc.isenabled()
+        gc.disable()
         if gate_s > 0:
-            # hold the stream while the host enqueues the steps, so that no
-            # launch waits on the host (small layers take less GPU time per
-            # step than the Python calls that enqueue it); outside the events
             torch.cuda._sleep(int(gate_s * 2.1e9))
         for i in range(n):
             self.flush()
@@ -526,6 +530,8 @@ class GpuCase:
             self.layer.combine(self.eo, self.wts, self.topk, self.lay, self.out)
             e[3].record(self.st)
         torch.cuda.synchronize(self.dev)
+        if gc_was:
+            gc.enable()
         status = self.layer.device_status()
         if status != 0:
             raise SystemExit(f"device status {status} in the timed region ({self.w.name})")

@@ -36,7 +36,7 @@ namespace {
 constexpr int kXTileSmall = 128;          // tokens per tile when E is large
 constexpr int kXTileLarge = 256;          // tokens per tile when E <= kXLargeMaxE
 constexpr int kXLargeMaxE = 2048;
-constexpr int kPickBatch = 8;             // picks whose loads are in flight together
+constexpr int kPickBatch = 4;             // picks whose loads are in flight together
 
 struct ExpertParams {
     const int32_t *topk_idx;
@@ -61,8 +61,10 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&v)[8]) {
                  : "memory");
 }
 
+// K <= 8: four CTAs per SM (at most 64 registers a thread at 256 threads), so
+// that a 512-tile layer runs in one wave.
 template <int KMAX, int TILE>
-__global__ void __launch_bounds__(TILE) expert_layout_kernel(const ExpertParams p) {
+__global__ void __launch_bounds__(TILE, KMAX <= 8 ? 4 : 1) expert_layout_kernel(const ExpertParams p) {
     constexpr int kXWords = TILE / 32;   // mask words per expert (one per warp)
     extern __shared__ __align__(16) uint32_t s_mask[];    // [E][kXWords], then s_excl[E]
     __shared__ unsigned long long s_ticket;

@@ -31,9 +31,10 @@
 //      which the last tile derives the per-(s, d) counts and all the small
 //      scans) and adds its histogram; fence; counts the tile done;
 //   5. writes token_slot, each thread its token's row in 16-byte stores --
-//      after the fence, which therefore does not wait for these stores; the
-//      last tile to finish then runs the small scans, with every load of a
-//      batch issued before the first is used.
+//      after the fence, which therefore does not wait for these stores.
+// One more CTA, the finisher (it draws the call's last ticket), waits until
+// every tile has counted itself done, brings the column prefixes and the
+// histogram into shared memory with bulk copies, and runs the small scans.
 #include <atomic>
 
 #include "ep_internal.cuh"
