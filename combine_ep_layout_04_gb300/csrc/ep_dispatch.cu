@@ -1359,8 +1359,20 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
     // dependent load per channel and destination.
     unsigned *chan = reinterpret_cast<unsigned *>(smem + L.chan_off);   // [C], prologue only
     long long n_recv = 0;
+    int err0 = 0;
     if (threadIdx.x < p.C) chan[threadIdx.x] = 0u;
+    // the first round of message-count loads, issued with the other prologue
+    // loads (one round trip for all of them); summed after the barrier
+    const int npairs = (p.s1 - p.s0) * p.R;
+    const int32_t *mc = p.msg_count + static_cast<int64_t>(p.s0) * p.R;
+    int v0[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int i = static_cast<int>(threadIdx.x) + q * kThreads;
+        v0[q] = i < npairs ? __ldg(mc + i) : 0;
+    }
     if (warp == 0 && lane == 0) {
+        err0 = read_error(p.dev.err);
         if (!channel_cta) {
             const int store_warps = p.vec_store ? p.store_warps : 1;
             for (int i = 0; i < p.stages; ++i) {
@@ -1402,24 +1414,22 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_kernel(const DispatchPar
         }
     }
     __syncthreads();
-    {
-        const int npairs = (p.s1 - p.s0) * p.R;
-        const int32_t *mc = p.msg_count + static_cast<int64_t>(p.s0) * p.R;
-        for (int i0 = threadIdx.x; i0 < npairs; i0 += 4 * kThreads) {
-            int v[4];
+    for (int i0 = threadIdx.x; i0 < npairs; i0 += 4 * kThreads) {
+        int v[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) v[q] = i0 + q * kThreads < npairs ? __ldg(mc + i0 + q * kThreads) : 0;
+        for (int q = 0; q < 4; ++q)
+            v[q] = i0 == static_cast<int>(threadIdx.x) ? v0[q]
+                   : (i0 + q * kThreads < npairs ? __ldg(mc + i0 + q * kThreads) : 0);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (v[q] != 0) atomicAdd(&chan[((i0 + q * kThreads) % p.R) % p.C], static_cast<unsigned>(v[q]));
-        }
+        for (int q = 0; q < 4; ++q)
+            if (v[q] != 0) atomicAdd(&chan[((i0 + q * kThreads) % p.R) % p.C], static_cast<unsigned>(v[q]));
     }
     __syncthreads();
     if (warp == 0 && lane == 0) {
         // N against the receive capacity; every channel's count against its log
         long long worst = 0;
         for (int c = 0; c < p.C; ++c) worst = max(worst, static_cast<long long>(chan[c]));
-        int abort = read_error(p.dev.err) != 0;
+        int abort = err0 != 0;
         if (n_recv > p.cap_rows || n_recv < 0) {
             set_error(p.dev.err, EP_ERR_CAPACITY);
             abort = 1;
