@@ -73,7 +73,10 @@ typedef struct {
     int32_t hidden;          /* H, multiple of 8; a row is 2*H bytes of bf16 */
     int32_t num_experts;     /* E, a multiple of R; expert e lives on rank e / (E/R) */
     int32_t topk;            /* K, 1..32 */
-    int32_t channels;        /* C, 1..64: rings; a message to rank d goes to ring d % C */
+    int32_t channels;        /* C, 1..64: rings; a message to rank d goes to ring d % C.
+                                The default is the tuning table's 8; a small layer's
+                                posting tail shrinks with more rings (the 32-rank,
+                                128-token layer: 108.6 us at 8, 100.7 at 16) */
     int32_t ring_depth;      /* D, power of two, 8..8192 slots per ring */
     int32_t max_inflight;    /* 8..D: producers wait while head - tail would exceed it */
     int32_t batch;           /* 1..8 commands reserved per head update */
